@@ -1,0 +1,102 @@
+/* tq.h -- C ABI of the GB300 TurboQuant KV-cache codec (libtq.so).
+ *
+ * The codec is the one on page "@mlx-bun/inference 0.0.0-stage -> 1.0.0",
+ * file package/src/kernels/turboquant/ops.ts, with the constants of page
+ * "mlx-bun 0.0.9 -> 0.0.11", file package/src/mlx/turboquant-tables.ts:
+ *   keys   -> per-32-group affine min/max quantisation along head_dim in fp32,
+ *             scale and zero point stored as fp16 (encodeKeys / decodeKeys);
+ *   values -> sign flip, normalised Hadamard transform, per-32-group RMS scale
+ *             (fp16), Lloyd-Max index (encodeValues / decodeValues);
+ *   codes  -> byte-aligned LSB-first bit packing per row (packBits / unpackBits).
+ *
+ * Conventions shared by every call:
+ *   - K and V tensors are contiguous [B, H, T, D] (batch, kv heads, tokens,
+ *     head_dim), element type tq_dtype.
+ *   - A packed cache is five contiguous buffers, each [B, H, t_cap, X]:
+ *       k_codes  X = tq_packed_dim(D, k_bits) bytes (int8 two's complement
+ *                when k_signed, else unsigned codes),
+ *       k_scales X = D/32 fp16, k_zeros X = D/32 fp16,
+ *       v_codes  X = tq_packed_dim(D, v_bits) bytes, v_scales X = D/32 fp16.
+ *     Rows (b, h, t) are packed independently, so a token is a whole row of
+ *     each buffer and appends never touch another token's bytes.
+ *   - All buffer pointers are device pointers owned by the caller; the library
+ *     never allocates, frees or keeps them. Every buffer pointer must be 16-byte
+ *     aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and runs asynchronously; the call returns once it is enqueued.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     non-OK status means nothing was enqueued, except TQ_ERR_CUDA, which
+ *     reports the launch error (cudaGetLastError) of the kernel just enqueued.
+ *   - Numerics: fp32 with one IEEE rounding per operation in the pages' order;
+ *     round() is round-half-to-even; fp16/bf16 stores round to nearest even.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, t_off + T > t_cap, size overflow */
+    TQ_ERR_HEAD_DIM = 2,    /* D not in {64, 128, 256, 512} */
+    TQ_ERR_BITS = 3,        /* v_bits not in {2,3,4,5,8}; k_bits not in {2,4,5,8};
+                               k_signed with k_bits != 8 */
+    TQ_ERR_ALIGNMENT = 4,   /* dim*bits not a multiple of 8; a buffer not 16-byte aligned */
+    TQ_ERR_DTYPE = 5,       /* unknown tq_dtype */
+    TQ_ERR_CUDA = 6         /* the CUDA runtime reported an error */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
+
+/* packedDim (ops.ts, packedDim): bytes of one packed row of `dim` codes of
+ * `bits` bits, dim*bits/8. Returns -TQ_ERR_ALIGNMENT when dim*bits is not a
+ * multiple of 8 and -TQ_ERR_INVALID_ARG for dim < 0 or bits < 1. */
+int64_t tq_packed_dim(int64_t dim, int bits);
+
+/* Encode (ops.ts: encodeKeys + packBits for K, encodeValues + packBits for V),
+ * one fused kernel.
+ *   k, v        [B,H,T,D] inputs of type in_dtype (read only).
+ *   k_bits      2, 4, 5 or 8; k_signed = 1 selects the symmetric int8 form
+ *               (k_bits must be 8).
+ *   v_bits      2, 3, 4, 5 or 8 (Lloyd-Max table width).
+ *   k_codes, k_scales, k_zeros, v_codes, v_scales: the packed cache, capacity
+ *               t_cap tokens; tokens [t_off, t_off + T) are written, nothing
+ *               else is touched.
+ * T == 0 (or B*H == 0) is a no-op that returns TQ_OK. */
+tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
+                       int64_t B, int64_t H, int64_t T, int64_t D,
+                       int k_bits, int k_signed, int v_bits,
+                       void* k_codes, void* k_scales, void* k_zeros,
+                       void* v_codes, void* v_scales,
+                       int64_t t_cap, int64_t t_off, void* stream);
+
+/* Decode (ops.ts: unpackBits + decodeKeys for K; unpackBits + decodeValues,
+ * i.e. centroid * scale followed by the inverse rotation, for V), one fused
+ * kernel. Reads tokens [0, T) of a cache of capacity t_cap >= T and writes
+ * k_out, v_out as contiguous [B,H,T,D] of type out_dtype. A key group whose
+ * stored zero point is infinite (a constant group, see the ops.ts header)
+ * decodes to NaN, as the page's formula (q + zero) * scale gives. */
+tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
+                       const void* v_codes, const void* v_scales,
+                       int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
+                       int k_bits, int k_signed, int v_bits,
+                       void* k_out, void* v_out, tq_dtype out_dtype, void* stream);
+
+/* Lloyd-Max index (ops.ts, searchsorted): idx[i] = number of boundaries of
+ * the v_bits table strictly below u[i] (NaN -> 0), for n fp32 values already
+ * in the rotated, RMS-normalised domain. u and idx are device pointers
+ * (u 4-byte aligned, idx unaligned bytes). The same device routine the
+ * encode kernel uses. */
+tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* tq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

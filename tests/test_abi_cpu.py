@@ -1,0 +1,122 @@
+"""The C ABI library without a GPU: it builds, loads, exports every function
+include/tq.h declares, and rejects bad arguments on the host before any CUDA
+call (so these checks run anywhere). Every call below is invalid by
+construction; none can reach a kernel launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tq.h")
+
+OK, INVALID, HEAD_DIM, BITS, ALIGN, DTYPE, CUDA = range(7)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from turboquant_kv_cache_tq_gb300 import build
+
+    build.build()
+    import turboquant_kv_cache_tq_gb300 as tq
+
+    return tq.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for n in ("tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_lloyd_max_index", "tq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L._name)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_packed_dim(L):
+    for d in (64, 128, 256, 512):
+        for b in (2, 3, 4, 5, 8):
+            assert L.tq_packed_dim(d, b) == d * b // 8
+    assert L.tq_packed_dim(512, 5) == 320 and L.tq_packed_dim(128, 3) == 48
+    assert L.tq_packed_dim(3, 3) == -ALIGN and L.tq_packed_dim(5, 5) == -ALIGN
+    assert L.tq_packed_dim(-1, 3) == -INVALID and L.tq_packed_dim(64, 0) == -INVALID
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.tq_status_string(s).startswith(b"TQ_")
+    assert b"unknown" in L.tq_status_string(99)
+
+
+def _enc(L, D=128, T=4, kb=8, ks=1, vb=3, dtype=1, t_cap=None, t_off=0, ptrs=None, B=1, H=2):
+    t_cap = T if t_cap is None else t_cap
+    ptrs = ptrs if ptrs is not None else [0] * 7
+    return L.tq_encode_kv(ptrs[0], ptrs[1], dtype, B, H, T, D, kb, ks, vb, *ptrs[2:], t_cap, t_off, None)
+
+
+def _dec(L, D=128, T=4, kb=8, ks=1, vb=3, dtype=1, t_cap=None, ptrs=None, B=1, H=2):
+    t_cap = T if t_cap is None else t_cap
+    ptrs = ptrs if ptrs is not None else [0] * 7
+    return L.tq_decode_kv(*ptrs[:5], B, H, T, D, t_cap, kb, ks, vb, ptrs[5], ptrs[6], dtype, None)
+
+
+@pytest.mark.parametrize("fn", [_enc, _dec])
+def test_argument_checks(L, fn):
+    assert fn(L, D=96) == HEAD_DIM and fn(L, D=32) == HEAD_DIM and fn(L, D=1024) == HEAD_DIM
+    assert fn(L, vb=6) == BITS and fn(L, vb=1) == BITS
+    assert fn(L, kb=3, ks=0) == BITS and fn(L, kb=4, ks=1) == BITS and fn(L, kb=16, ks=0) == BITS
+    assert fn(L, dtype=7) == DTYPE
+    assert fn(L, T=-1) == INVALID and fn(L, B=-2) == INVALID
+    assert fn(L, T=8, t_cap=4) == INVALID
+    # null buffers with work to do
+    assert fn(L) == INVALID
+    # empty work is a no-op, even with null buffers
+    assert fn(L, T=0) == OK and fn(L, B=0) == OK and fn(L, H=0) == OK
+
+
+def test_encode_offset_checks(L):
+    assert _enc(L, T=4, t_cap=5, t_off=2) == INVALID
+    assert _enc(L, T=4, t_cap=8, t_off=-1) == INVALID
+    assert _enc(L, T=0, t_cap=8, t_off=8) == OK
+
+
+def test_misaligned_buffers_rejected(L):
+    # one misaligned pointer among non-null ones: the check fires before launch
+    base = 1 << 20
+    ptrs = [base + 256 * i for i in range(7)]
+    for i in range(7):
+        bad = list(ptrs)
+        bad[i] += 8
+        assert _enc(L, ptrs=bad) == ALIGN
+        assert _dec(L, ptrs=bad) == ALIGN
+
+
+def test_size_overflow_rejected(L):
+    assert _enc(L, B=1 << 20, H=1 << 20, T=1 << 12) == INVALID
+    assert _dec(L, T=1 << 31, t_cap=1 << 31) == INVALID
+
+
+def test_lloyd_max_index_checks(L):
+    assert L.tq_lloyd_max_index(None, 0, 3, None, None) == OK
+    assert L.tq_lloyd_max_index(None, 5, 6, None, None) == BITS
+    assert L.tq_lloyd_max_index(None, -1, 3, None, None) == INVALID
+    assert L.tq_lloyd_max_index(None, 5, 3, None, None) == INVALID
+    assert L.tq_lloyd_max_index(1 << 20 | 2, 5, 3, 1 << 21, None) == ALIGN
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import turboquant_kv_cache_tq_gb300 as tq
+
+    monkeypatch.setattr(tq, "_lib", None)
+    monkeypatch.setattr(tq, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        tq.lib()

@@ -1,0 +1,168 @@
+"""GB300 TurboQuant KV-cache codec: Python binding of the C ABI in include/tq.h.
+
+This module only marshals torch tensors (device pointers, sizes and the
+current CUDA stream) into ``libtq.so``; every step of encode and decode runs
+in the library's CUDA kernels. There is no fallback: if the library is not
+built, importing works but every call raises.
+
+Names follow the C ABI: ``tq_packed_dim``, ``tq_encode_kv``, ``tq_decode_kv``,
+``tq_lloyd_max_index``, ``tq_status_string``; ``alloc_cache`` allocates the
+five packed-cache buffers with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_lloyd_max_index",
+    "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtq.so")
+HEAD_DIMS = (64, 128, 256, 512)
+VALUE_BITS = (2, 3, 4, 5, 8)
+KEY_MODES = ((2, False), (4, False), (5, False), (8, False), (8, True))
+GROUP = 32
+TQ_F32, TQ_BF16 = 0, 1
+_DTYPE = {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16}
+_NAMES = ("TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_ALIGNMENT",
+          "TQ_ERR_DTYPE", "TQ_ERR_CUDA")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TQError(RuntimeError):
+    """A non-OK tq_status from the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = _NAMES[status] if 0 <= status < len(_NAMES) else str(status)
+        super().__init__("%s: %s (%s)" % (what, name, tq_status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "libtq.so is not built (%s); run python -m turboquant_kv_cache_tq_gb300.build" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            L.tq_packed_dim.restype = I64
+            L.tq_packed_dim.argtypes = [I64, I]
+            L.tq_encode_kv.restype = I
+            L.tq_encode_kv.argtypes = [P, P, I, I64, I64, I64, I64, I, I, I, P, P, P, P, P, I64, I64, P]
+            L.tq_decode_kv.restype = I
+            L.tq_decode_kv.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
+            L.tq_lloyd_max_index.restype = I
+            L.tq_lloyd_max_index.argtypes = [P, I64, I, P, P]
+            L.tq_status_string.restype = ctypes.c_char_p
+            L.tq_status_string.argtypes = [I]
+            _lib = L
+    return _lib
+
+
+def tq_status_string(status: int) -> str:
+    return lib().tq_status_string(int(status)).decode()
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise TQError(status, what)
+
+
+def tq_packed_dim(dim: int, bits: int) -> int:
+    """Bytes of one packed row of `dim` codes at `bits` bits (raises if not byte-aligned)."""
+    r = int(lib().tq_packed_dim(int(dim), int(bits)))
+    if r < 0:
+        raise TQError(-r, "tq_packed_dim(%d, %d)" % (dim, bits))
+    return r
+
+
+def alloc_cache(B: int, H: int, t_cap: int, D: int, k_bits: int, v_bits: int, device="cuda") -> dict:
+    """The five packed-cache buffers [B,H,t_cap,X] (codes uint8, scales/zeros fp16)."""
+    G = D // GROUP
+    return dict(
+        k_codes=torch.zeros((B, H, t_cap, tq_packed_dim(D, k_bits)), dtype=torch.uint8, device=device),
+        k_scales=torch.zeros((B, H, t_cap, G), dtype=torch.float16, device=device),
+        k_zeros=torch.zeros((B, H, t_cap, G), dtype=torch.float16, device=device),
+        v_codes=torch.zeros((B, H, t_cap, tq_packed_dim(D, v_bits)), dtype=torch.uint8, device=device),
+        v_scales=torch.zeros((B, H, t_cap, G), dtype=torch.float16, device=device),
+    )
+
+
+def _cache_ptrs(cache: dict):
+    for name in ("k_codes", "k_scales", "k_zeros", "v_codes", "v_scales"):
+        t = cache[name]
+        if not t.is_contiguous():
+            raise ValueError("cache buffer %s must be contiguous" % name)
+    return [cache[n].data_ptr() for n in ("k_codes", "k_scales", "k_zeros", "v_codes", "v_scales")]
+
+
+def tq_encode_kv(k: torch.Tensor, v: torch.Tensor, k_bits: int, k_signed: bool, v_bits: int,
+                 cache: dict, t_off: int = 0, stream=None) -> dict:
+    """Encode K, V [B,H,T,D] (fp32 or bf16, contiguous, on the GPU) into tokens
+    [t_off, t_off+T) of `cache` (capacity = its token axis). Asynchronous on
+    `stream` (default: the current stream)."""
+    if k.shape != v.shape or k.dtype != v.dtype or k.dim() != 4:
+        raise ValueError("K and V must be [B,H,T,D] tensors of one shape and dtype")
+    if k.dtype not in _DTYPE:
+        raise ValueError("K/V dtype must be float32 or bfloat16, got %s" % k.dtype)
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("K and V must be contiguous")
+    B, H, T, D = k.shape
+    t_cap = cache["k_codes"].shape[2]
+    st = lib().tq_encode_kv(k.data_ptr(), v.data_ptr(), _DTYPE[k.dtype], B, H, T, D, int(k_bits),
+                            int(bool(k_signed)), int(v_bits), *_cache_ptrs(cache), t_cap, int(t_off),
+                            _stream_handle(stream, k.device))
+    _check(st, "tq_encode_kv")
+    return cache
+
+
+def tq_decode_kv(cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
+                 out_dtype=torch.bfloat16, k_out=None, v_out=None, stream=None):
+    """Decode tokens [0,T) of `cache` into K, V [B,H,T,D] of `out_dtype`
+    (allocated when not given). Asynchronous on `stream`."""
+    B, H, t_cap, _ = cache["k_codes"].shape
+    D = cache["k_scales"].shape[-1] * GROUP
+    dev = cache["k_codes"].device
+    if out_dtype not in _DTYPE:
+        raise ValueError("out_dtype must be float32 or bfloat16")
+    if k_out is None:
+        k_out = torch.empty((B, H, T, D), dtype=out_dtype, device=dev)
+    if v_out is None:
+        v_out = torch.empty((B, H, T, D), dtype=out_dtype, device=dev)
+    for t in (k_out, v_out):
+        if t.dtype != out_dtype or tuple(t.shape) != (B, H, T, D) or not t.is_contiguous():
+            raise ValueError("k_out/v_out must be contiguous [B,H,T,D] tensors of out_dtype")
+    st = lib().tq_decode_kv(*_cache_ptrs(cache), B, H, T, D, t_cap, int(k_bits), int(bool(k_signed)),
+                            int(v_bits), k_out.data_ptr(), v_out.data_ptr(), _DTYPE[out_dtype],
+                            _stream_handle(stream, dev))
+    _check(st, "tq_decode_kv")
+    return k_out, v_out
+
+
+def tq_lloyd_max_index(u: torch.Tensor, v_bits: int, out=None, stream=None) -> torch.Tensor:
+    """count(boundaries < u) for each fp32 element of `u` (uint8 result)."""
+    if u.dtype != torch.float32 or not u.is_contiguous():
+        raise ValueError("u must be a contiguous float32 tensor")
+    if out is None:
+        out = torch.empty(u.shape, dtype=torch.uint8, device=u.device)
+    st = lib().tq_lloyd_max_index(u.data_ptr(), u.numel(), int(v_bits), out.data_ptr(),
+                                  _stream_handle(stream, u.device))
+    _check(st, "tq_lloyd_max_index")
+    return out

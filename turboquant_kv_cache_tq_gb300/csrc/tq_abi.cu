@@ -1,0 +1,210 @@
+// C ABI of the TurboQuant KV codec (declared in include/tq.h): argument
+// checks on the host, then one fused kernel per call on the caller's stream.
+// Page "@mlx-bun/inference 0.0.0-stage -> 1.0.0", file
+// package/src/kernels/turboquant/ops.ts: packedDim throws on a non-byte-aligned
+// size, fwht rejects unsupported head dims, the Lloyd-Max tables exist for
+// 2/3/4/5/8 bits and signed keys exist only at 8 bits; each of those becomes a
+// status code returned before any launch.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/tq.h"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+int sm_count() {
+  static int cached[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+__global__ void lloyd_max_index_kernel(const float* u, long long n, int v_bits, uint8_t* idx) {
+  __shared__ CellEntry s_cells[CellGrid<8>::n];
+  const CellEntry* tab = v_bits == 4 ? cell_table<4>() : v_bits == 5 ? cell_table<5>() : cell_table<8>();
+  const int nc = v_bits == 4 ? CellGrid<4>::n : v_bits == 5 ? CellGrid<5>::n : CellGrid<8>::n;
+  if (v_bits >= 4) {
+    for (int i = threadIdx.x; i < nc; i += blockDim.x) s_cells[i] = tab[i];
+  }
+  __syncthreads();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride) {
+    const float x = u[i];
+    int r;
+    switch (v_bits) {
+      case 2: r = lm_index<2>(x, s_cells); break;
+      case 3: r = lm_index<3>(x, s_cells); break;
+      case 4: r = lm_index<4>(x, s_cells); break;
+      case 5: r = lm_index<5>(x, s_cells); break;
+      default: r = lm_index<8>(x, s_cells); break;
+    }
+    idx[i] = static_cast<uint8_t>(r);
+  }
+}
+
+bool head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+bool value_bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 8; }
+
+// Key mode of (bits, signed), or -1.
+int key_mode(int bits, int is_signed) {
+  if (is_signed) return bits == 8 ? kK8Signed : -1;
+  switch (bits) {
+    case 2: return kK2;
+    case 4: return kK4;
+    case 5: return kK5;
+    case 8: return kK8;
+    default: return -1;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks of encode and decode; fills rows.
+tq_status check_common(int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap, int64_t t_off,
+                       int k_bits, int k_signed, int v_bits, int dtype, long long* rows) {
+  if (B < 0 || H < 0 || T < 0 || t_cap < 0 || t_off < 0) return TQ_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return TQ_ERR_HEAD_DIM;
+  if (key_mode(k_bits, k_signed) < 0 || !value_bits_ok(v_bits)) return TQ_ERR_BITS;
+  if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_DTYPE;
+  if (t_off > t_cap || T > t_cap - t_off) return TQ_ERR_INVALID_ARG;
+  // Row indices and per-(b,h) token counts are 32-bit inside the kernels.
+  const long long lim = 0x7fffffffLL;
+  if (T > lim || t_cap > lim) return TQ_ERR_INVALID_ARG;
+  if (B > lim || H > lim || (B > 0 && H > lim / B)) return TQ_ERR_INVALID_ARG;
+  const long long bh = B * H;
+  if (bh > 0 && T > lim / bh) return TQ_ERR_INVALID_ARG;
+  if (bh > 0 && t_cap > (1LL << 62) / (bh * 512)) return TQ_ERR_INVALID_ARG;
+  *rows = bh * T;
+  return TQ_OK;
+}
+
+float rotation_scale(int64_t d) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))); }
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" int64_t tq_packed_dim(int64_t dim, int bits) {
+  if (dim < 0 || bits < 1) return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
+  if (dim > (INT64_MAX / 64)) return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
+  if ((dim * bits) % 8 != 0) return -static_cast<int64_t>(TQ_ERR_ALIGNMENT);
+  return dim * bits / 8;
+}
+
+extern "C" tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
+                                  int64_t B, int64_t H, int64_t T, int64_t D,
+                                  int k_bits, int k_signed, int v_bits,
+                                  void* k_codes, void* k_scales, void* k_zeros,
+                                  void* v_codes, void* v_scales,
+                                  int64_t t_cap, int64_t t_off, void* stream) {
+  long long rows = 0;
+  const tq_status st = check_common(B, H, T, D, t_cap, t_off, k_bits, k_signed, v_bits,
+                                    static_cast<int>(in_dtype), &rows);
+  if (st != TQ_OK) return st;
+  if (rows == 0) return TQ_OK;
+  const void* ptrs[] = {k, v, k_codes, k_scales, k_zeros, v_codes, v_scales};
+  for (const void* p : ptrs) {
+    if (!p) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TQ_ERR_ALIGNMENT;
+  }
+  EncodeParams p{};
+  p.k = k;
+  p.v = v;
+  p.k_codes = static_cast<uint8_t*>(k_codes);
+  p.k_scales = static_cast<uint16_t*>(k_scales);
+  p.k_zeros = static_cast<uint16_t*>(k_zeros);
+  p.v_codes = static_cast<uint8_t*>(v_codes);
+  p.v_scales = static_cast<uint16_t*>(v_scales);
+  p.rows = static_cast<int>(rows);
+  p.T = static_cast<int>(T);
+  p.t_cap = t_cap;
+  p.t_off = t_off;
+  p.kmode = key_mode(k_bits, k_signed);
+  p.rot_scale = rotation_scale(D);
+  const bool bf16 = in_dtype == TQ_BF16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_encode<64>(p, v_bits, bf16, s); break;
+    case 128: e = launch_encode<128>(p, v_bits, bf16, s); break;
+    case 256: e = launch_encode<256>(p, v_bits, bf16, s); break;
+    default: e = launch_encode<512>(p, v_bits, bf16, s); break;
+  }
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
+                                  const void* v_codes, const void* v_scales,
+                                  int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
+                                  int k_bits, int k_signed, int v_bits,
+                                  void* k_out, void* v_out, tq_dtype out_dtype, void* stream) {
+  long long rows = 0;
+  const tq_status st = check_common(B, H, T, D, t_cap, 0, k_bits, k_signed, v_bits,
+                                    static_cast<int>(out_dtype), &rows);
+  if (st != TQ_OK) return st;
+  if (rows == 0) return TQ_OK;
+  const void* ptrs[] = {k_codes, k_scales, k_zeros, v_codes, v_scales, k_out, v_out};
+  for (const void* p : ptrs) {
+    if (!p) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TQ_ERR_ALIGNMENT;
+  }
+  DecodeParams p{};
+  p.k_codes = static_cast<const uint8_t*>(k_codes);
+  p.k_scales = static_cast<const uint16_t*>(k_scales);
+  p.k_zeros = static_cast<const uint16_t*>(k_zeros);
+  p.v_codes = static_cast<const uint8_t*>(v_codes);
+  p.v_scales = static_cast<const uint16_t*>(v_scales);
+  p.k_out = k_out;
+  p.v_out = v_out;
+  p.rows = static_cast<int>(rows);
+  p.T = static_cast<int>(T);
+  p.t_cap = t_cap;
+  p.kmode = key_mode(k_bits, k_signed);
+  p.rot_scale = rotation_scale(D);
+  const bool bf16 = out_dtype == TQ_BF16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_decode<64>(p, v_bits, bf16, s); break;
+    case 128: e = launch_decode<128>(p, v_bits, bf16, s); break;
+    case 256: e = launch_decode<256>(p, v_bits, bf16, s); break;
+    default: e = launch_decode<512>(p, v_bits, bf16, s); break;
+  }
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx, void* stream) {
+  if (n < 0) return TQ_ERR_INVALID_ARG;
+  if (!value_bits_ok(v_bits)) return TQ_ERR_BITS;
+  if (n == 0) return TQ_OK;
+  if (!u || !idx) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(u) & 3u) != 0) return TQ_ERR_ALIGNMENT;
+  const long long blocks_needed = (n + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
+  lloyd_max_index_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(u, n, v_bits, idx);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" const char* tq_status_string(int status) {
+  switch (status) {
+    case TQ_OK: return "TQ_OK";
+    case TQ_ERR_INVALID_ARG: return "TQ_ERR_INVALID_ARG: null pointer, negative or inconsistent size";
+    case TQ_ERR_HEAD_DIM: return "TQ_ERR_HEAD_DIM: head_dim must be 64, 128, 256 or 512";
+    case TQ_ERR_BITS: return "TQ_ERR_BITS: v_bits in {2,3,4,5,8}, k_bits in {2,4,5,8}, signed keys need 8 bits";
+    case TQ_ERR_ALIGNMENT: return "TQ_ERR_ALIGNMENT: size not byte-aligned or buffer not 16-byte aligned";
+    case TQ_ERR_DTYPE: return "TQ_ERR_DTYPE: dtype must be TQ_F32 or TQ_BF16";
+    case TQ_ERR_CUDA: return "TQ_ERR_CUDA: the CUDA runtime reported an error";
+    default: return "unknown tq_status";
+  }
+}

@@ -1,0 +1,55 @@
+// Internal launch interface between the C ABI (tq_abi.cu) and the per-head_dim
+// kernel translation units (tq_kernels_d*.cu). Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tq {
+
+// Key modes: (bits, signed) pairs the key path supports.
+enum KeyMode : int { kK2 = 0, kK4 = 1, kK5 = 2, kK8 = 3, kK8Signed = 4 };
+
+struct EncodeParams {
+  const void* k;        // [rows, D] inputs (fp32 or bf16)
+  const void* v;
+  uint8_t* k_codes;     // [B*H, t_cap, pd(D, k_bits)]
+  uint16_t* k_scales;   // [B*H, t_cap, D/32] fp16 bits
+  uint16_t* k_zeros;
+  uint8_t* v_codes;     // [B*H, t_cap, pd(D, v_bits)]
+  uint16_t* v_scales;
+  int rows;             // B*H*T
+  int T;                // tokens per (b, h) in the input
+  long long t_cap;      // cache capacity in tokens
+  long long t_off;      // first cache token written
+  int kmode;            // KeyMode
+  float rot_scale;      // fp32(1/sqrt(D))
+};
+
+struct DecodeParams {
+  const uint8_t* k_codes;
+  const uint16_t* k_scales;
+  const uint16_t* k_zeros;
+  const uint8_t* v_codes;
+  const uint16_t* v_scales;
+  void* k_out;          // [rows, D] outputs (fp32 or bf16)
+  void* v_out;
+  int rows;             // B*H*T
+  int T;                // tokens decoded per (b, h)
+  long long t_cap;
+  int kmode;
+  float rot_scale;
+};
+
+// One launcher per head_dim (tq_kernels_d<D>.cu); v_bits in {2,3,4,5,8}.
+template <int D>
+cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaStream_t s);
+template <int D>
+cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, cudaStream_t s);
+
+cudaError_t launch_lloyd_max_index(const float* u, long long n, int v_bits, uint8_t* idx, cudaStream_t s);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+}  // namespace tq
