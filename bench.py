@@ -1,0 +1,410 @@
+"""Benchmark of the GB300 TurboQuant KV codec: encode + decode throughput.
+
+One step = encode then decode of the KV cache of every layer of a
+Llama-3-8B-shaped model for one 4096-token sequence: 32 layers of K, V
+[1, 8, 4096, 128] bf16 (N(0,1) with 1% outliers x10), keys 8-bit signed,
+values 3-bit. Every layer has its own inputs, packed cache and decoded outputs
+(about 1.3 GB in all, ten times the L2), so each launch streams from HBM.
+The metric is layer-tokens per second: one token = one (batch, position) of
+one layer, all 8 KV heads, K and V, encoded and decoded.
+
+Output: one JSON line (rank 0). Fields beyond the metric:
+  roofline      the dominant kernel's algorithmic bytes per launch over its
+                average launch time (CUDA events on its stream), against the
+                measured HBM copy bandwidth (MEASURED_PEAKS.json);
+  e2e           the same metric through the Python API with pinned host
+                buffers: host->device copy of the inputs and device->host
+                copy of the decoded K, V inside the timed region;
+  cpu_baseline  the oracle (single-threaded C) on a bounded sample of the
+                same workload, on this machine's host cores;
+  clocks        nvidia-smi samples taken during the timed region.
+``--impl reference`` times the oracle alone as the reference arm.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(weak scaling; the codec has no cross-row exchange), timed between barriers,
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 32
+WORKLOAD = "llama3_8b_layer"
+METRIC = "TurboQuant KV encode/decode tokens/s; achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---- multi-rank plumbing (host logic; tested with gloo on CPU) --------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(backend: str):
+    rank, ws, _ = dist_env()
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return rank, ws
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, device="cpu") -> float:
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- byte accounting ------------------------------------------------------------
+def bytes_per_row(D: int, k_bits: int, v_bits: int, io_bytes: int) -> int:
+    """Algorithmic HBM bytes of one (b,h,t) row for encode (and for decode):
+    K and V rows in (out), packed K and V codes, fp16 K scale + zero and V scale."""
+    G = D // 32
+    return 2 * D * io_bytes + D * k_bits // 8 + D * v_bits // 8 + 2 * G * 2 + G * 2
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "turboquant_kv_cache_tq_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---- clocks -----------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        mx = [float(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        loaded = [s for s, r in zip(sm, rows) if float(r[3]) > 200.0] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- CPU baseline (the oracle) ------------------------------------------------------
+def oracle_timing(rows_target: int, min_seconds: float, max_seconds: float):
+    """Time the oracle's encode + decode on row chunks of the workload until
+    min_seconds have passed; returns (rows, seconds)."""
+    import numpy as np
+
+    import oracle
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv, to_oracle
+
+    w = WORKLOADS[WORKLOAD]
+    chunk_T = 256
+    k, v = make_kv(w, T=chunk_T)  # [1, 8, 256, 128]: 2048 rows per chunk
+    ko, vo = to_oracle(k), to_oracle(v)
+    oracle.lib()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        cache = oracle.encode_kv(ko, vo, w.k_bits, w.k_signed, w.v_bits[0])
+        oracle.decode_kv(cache, chunk_T, w.k_bits, w.k_signed, w.v_bits[0], out_dtype=oracle.BF16)
+        done += ko.shape[1] * chunk_T
+        el = time.perf_counter() - t0
+        if (el >= min_seconds and done >= min(rows_target, 2048)) or el >= max_seconds:
+            return done, el
+
+
+def run_reference(args):
+    """The reference arm: the oracle, timed as it stands on the host cores."""
+    rank, ws, _ = dist_env()
+    if rank != 0:
+        return
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[WORKLOAD]
+    per_step_budget = max(0.02, 150.0 / max(1, args.steps + args.warmup))
+    # calibrate: rows the oracle encodes + decodes per second
+    rows, secs = oracle_timing(2048, 0.5, 5.0)
+    rate = rows / secs
+    step_rows = max(2048, int(rate * per_step_budget) // 2048 * 2048)
+    for _ in range(args.warmup):
+        oracle_timing(step_rows, 0.0, per_step_budget * 2)
+    total_rows, total_s = 0, 0.0
+    for _ in range(args.steps):
+        r, s = oracle_timing(step_rows, per_step_budget, per_step_budget * 4)
+        total_rows += r
+        total_s += s
+    tokens = total_rows / w.H
+    value = tokens / total_s
+    per_step = total_rows // max(1, args.steps)
+    sample = ("%d rows (%d tokens) of %s per step on average, encode+decode, bf16 out, single-threaded"
+              % (per_step, per_step // w.H, WORKLOAD))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shape": [w.B, w.H, w.T, w.D], "k_bits": 8, "k_signed": True,
+                   "v_bits": 3, "in_dtype": "bf16", "out_dtype": "bf16"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- the GPU arm --------------------------------------------------------------------
+def run_ours(args):
+    import turboquant_kv_cache_tq_gb300 as tq
+    from turboquant_kv_cache_tq_gb300 import build as tq_build
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv
+
+    rank, ws, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    rank, ws = init_dist("nccl")
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(tq.LIB_PATH):
+        tq_build.build()
+    barrier()
+    tq.lib()
+
+    w = WORKLOADS[WORKLOAD]
+    kb, ks, vb = w.k_bits, w.k_signed, w.v_bits[0]
+    B, H, T, D = w.B, w.H, w.T, w.D
+    layers = []
+    for i in range(LAYERS):
+        k, v = make_kv(w, device=dev, seed=1000 * (rank + 1) + i)
+        layers.append(dict(k=k, v=v, cache=tq.alloc_cache(B, H, T, D, kb, vb, device=dev),
+                           ko=torch.empty_like(k), vo=torch.empty_like(v)))
+    stream = torch.cuda.Stream(device=dev)
+
+    def enc_all():
+        for L in layers:
+            tq.tq_encode_kv(L["k"], L["v"], kb, ks, vb, L["cache"], stream=stream)
+
+    def dec_all():
+        for L in layers:
+            tq.tq_decode_kv(L["cache"], T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=L["ko"], v_out=L["vo"],
+                            stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            enc_all()
+            dec_all()
+    torch.cuda.synchronize(dev)
+    g_enc, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_enc, stream=stream):
+        enc_all()
+    with torch.cuda.graph(g_dec, stream=stream):
+        dec_all()
+    torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_enc.replay()
+            g_dec.replay()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            for e in ev:
+                e[0].record(stream)
+                g_enc.replay()
+                e[1].record(stream)
+                g_dec.replay()
+                e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    enc_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    clocks = clk.summary()
+    total_ms = max_over_ranks(total_ms, dev)
+
+    tokens_per_step = B * T * LAYERS
+    value = tokens_per_step * args.steps * ws / (total_ms / 1e3)
+    rows = B * H * T
+    bpl = rows * bytes_per_row(D, kb, vb, 2)
+    enc_launch_us = 1e3 * enc_ms / (args.steps * LAYERS)
+    dec_launch_us = 1e3 * dec_ms / (args.steps * LAYERS)
+    dominant = "encode" if enc_ms >= dec_ms else "decode"
+    launch_us = max(enc_launch_us, dec_launch_us)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = bpl / (launch_us * 1e-6) / 1e9
+    kernel_name = "encode_kernel" if dominant == "encode" else "decode_kernel"
+
+    # ---- e2e through the Python API with pinned host buffers
+    e2e = run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream)
+    e2e_ms = max_over_ranks(e2e["ms"], dev)
+    e2e_value = tokens_per_step * e2e["steps"] * ws / (e2e_ms / 1e3)
+
+    cpu = None
+    if rank == 0 and ws == 1:
+        rows_done, secs = oracle_timing(rows, args.cpu_seconds, 3 * args.cpu_seconds)
+        cpu = {"value": rows_done / H / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "%d rows (%d tokens) of %s, encode+decode, bf16 out, single-threaded"
+                         % (rows_done, rows_done // H, WORKLOAD)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers_per_step": LAYERS, "shape": [B, H, T, D],
+                       "k_bits": kb, "k_signed": ks, "v_bits": vb, "in_dtype": "bf16", "out_dtype": "bf16",
+                       "l2": "inputs larger than L2: every layer has its own inputs, cache and outputs "
+                             "(%.2f GB)" % (LAYERS * (4 * rows * D * 2 + rows * (bpl // rows - 4 * D)) / 1e9),
+                       "timing": "CUDA graphs of the 32 encode and 32 decode launches, CUDA events"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(kernel_name),
+                         "kernel": kernel_name, "peak_source": peak_kind,
+                         "bytes_per_launch": bpl, "launch_us": launch_us},
+            "kernels": {"encode_us_per_launch": enc_launch_us, "decode_us_per_launch": dec_launch_us,
+                        "encode_GBps": bpl / (enc_launch_us * 1e-6) / 1e9,
+                        "decode_GBps": bpl / (dec_launch_us * 1e-6) / 1e9},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
+                    "d2h_bytes_per_step": e2e["d2h"]},
+            "cpu_baseline": cpu,
+            "gpu_launches": 2 * LAYERS * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    barrier()
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
+    """Host buffers in, host buffers out, through the Python API."""
+    host_in = [(L["k"].cpu().pin_memory(), L["v"].cpu().pin_memory()) for L in layers]
+    host_out = [(torch.empty_like(a).pin_memory(), torch.empty_like(b).pin_memory()) for a, b in host_in]
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def step():
+        for L, (hk, hv), (ok, ov) in zip(layers, host_in, host_out):
+            L["k"].copy_(hk, non_blocking=True)
+            L["v"].copy_(hv, non_blocking=True)
+            tq.tq_encode_kv(L["k"], L["v"], kb, ks, vb, L["cache"], stream=stream)
+            tq.tq_decode_kv(L["cache"], T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=L["ko"], v_out=L["vo"],
+                            stream=stream)
+            ok.copy_(L["ko"], non_blocking=True)
+            ov.copy_(L["vo"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    e1.synchronize()
+    barrier()
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_in)
+    d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_out)
+    return {"ms": e0.elapsed_time(e1), "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

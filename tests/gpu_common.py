@@ -1,0 +1,168 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+and the oracle on the same seeded inputs, and compare.
+
+Acceptance (element by element):
+- packed K codes, K scales, K zeros and V scales: bit-exact;
+- packed V codes: bit-exact, except indices whose normalised rotated value u
+  lies within 1e-5 of a Lloyd-Max boundary (at most 1e-4 of the elements);
+- decoded tensors: within 1e-5 relative error in fp32 (NaN where the oracle
+  has NaN), and bf16 outputs equal to the round-to-nearest-even of the
+  oracle's fp32 result (ties of that rounding are not reachable off by one:
+  the fp32 values must already agree to 1e-5).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import turboquant_kv_cache_tq_gb300 as tq
+from turboquant_kv_cache_tq_gb300.workloads import to_oracle
+
+V_TOL = 1e-5
+V_MAX_FRAC = 1e-4
+DEC_RTOL = 1e-5
+
+CACHE_KEYS = ("k_codes", "k_scales", "k_zeros", "v_codes", "v_scales")
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from turboquant_kv_cache_tq_gb300 import build
+
+    build.build()
+    return tq.lib()
+
+
+def cache_to_numpy(cache: dict) -> dict:
+    out = {}
+    for k in CACHE_KEYS:
+        t = cache[k].detach().cpu().contiguous()
+        out[k] = t.numpy() if t.dtype == torch.uint8 else t.view(torch.int16).numpy().view(np.uint16)
+    return out
+
+
+def cache_from_numpy(c: dict, device="cuda") -> dict:
+    out = {}
+    for k in CACHE_KEYS:
+        a = np.ascontiguousarray(c[k])
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        out[k] = (t.view(torch.float16) if a.dtype == np.uint16 else t).to(device)
+    return out
+
+
+def gpu_encode(k, v, k_bits, k_signed, v_bits, t_cap=None, t_off=0, cache=None, fill=None):
+    kd, vd = k.cuda(), v.cuda()
+    B, H, T, D = k.shape
+    if cache is None:
+        cache = tq.alloc_cache(B, H, T if t_cap is None else t_cap, D, k_bits, v_bits)
+        if fill is not None:
+            for t in cache.values():
+                t.view(torch.uint8).fill_(fill)
+    tq.tq_encode_kv(kd, vd, k_bits, k_signed, v_bits, cache, t_off=t_off)
+    torch.cuda.synchronize()
+    return cache
+
+
+def _unpack_rows(packed, bits, d):
+    return oracle.unpack_bits(packed.reshape(-1, packed.shape[-1]), bits, d)
+
+
+def rotated_normalised(v_np, v_scales_bits, d):
+    """u = fwht(v) / (fp32 rms + eps) per element, recomputed with the oracle's
+    rotation and the stored fp16 scale (only used to classify mismatches)."""
+    x = v_np if v_np.dtype == np.float32 else oracle.bf16_bits_to_f32(v_np)
+    y = oracle.fwht(x.reshape(-1, d), encode=True).astype(np.float64)
+    r = oracle.f16_bits_to_f32(v_scales_bits.reshape(-1, d // 32)).astype(np.float64)
+    return y / (np.repeat(r, 32, axis=1) + 1e-8)
+
+
+def compare_encoded(gpu: dict, ref: dict, D: int, v_bits: int, v_input=None, rows=None):
+    """Assert the acceptance rules on two packed caches (numpy dicts), either on
+    all rows or on the selected cache rows `rows` (indices into B*H*t_cap)."""
+    def sel(a):
+        a = a.reshape(-1, a.shape[-1])
+        return a if rows is None else a[rows]
+
+    for key in ("k_codes", "k_scales", "k_zeros", "v_scales"):
+        g, r = sel(gpu[key]), sel(ref[key])
+        if not np.array_equal(g, r):
+            bad = np.argwhere(g != r)
+            raise AssertionError("%s differs at %d places, first %s: gpu %s ref %s"
+                                 % (key, len(bad), bad[0].tolist(), g[tuple(bad[0])], r[tuple(bad[0])]))
+    g, r = sel(gpu["v_codes"]), sel(ref["v_codes"])
+    if np.array_equal(g, r):
+        return 0
+    gi = _unpack_rows(g, v_bits, D)
+    ri = _unpack_rows(r, v_bits, D)
+    mism = np.argwhere(gi != ri)
+    assert v_input is not None, "V codes differ and no input given to classify them"
+    u = rotated_normalised(v_input, sel(ref["v_scales"]), D)
+    _, bnd = oracle.lloyd_max(v_bits)
+    for (row, e) in mism:
+        dist = np.min(np.abs(u[row, e] - bnd.astype(np.float64)))
+        assert dist <= V_TOL, "V index differs at row %d elem %d (gpu %d, ref %d, |u-b| = %g)" % (
+            row, e, gi[row, e], ri[row, e], dist)
+    assert len(mism) <= max(1, V_MAX_FRAC * gi.size), "%d V index mismatches" % len(mism)
+    return len(mism)
+
+
+def compare_decoded(gpu: np.ndarray, ref: np.ndarray, what: str):
+    """fp32: NaN positions equal, |g - r| <= 1e-5 |r| elsewhere."""
+    g = gpu.astype(np.float64)
+    r = ref.astype(np.float64)
+    gn, rn = np.isnan(g), np.isnan(r)
+    assert np.array_equal(gn, rn), "%s: NaN positions differ (%d vs %d)" % (what, gn.sum(), rn.sum())
+    ok = ~rn
+    err = np.abs(g[ok] - r[ok])
+    lim = DEC_RTOL * np.abs(r[ok])
+    if not np.all((err <= lim) | (err == 0)):
+        i = np.argmax(err - lim)
+        raise AssertionError("%s: relative error above 1e-5 (gpu %r ref %r)" % (what, g[ok][i], r[ok][i]))
+    return int(np.count_nonzero(err))
+
+
+def oracle_encode(k, v, k_bits, k_signed, v_bits, t_cap=None, t_off=0, cache=None):
+    return oracle.encode_kv(to_oracle(k), to_oracle(v), k_bits, k_signed, v_bits, cache=cache,
+                            t_cap=t_cap, t_off=t_off)
+
+
+def check_roundtrip(k, v, k_bits, k_signed, v_bits, t_cap=None, t_off=0):
+    """Encode on both sides, compare; decode the oracle's bytes on both sides
+    (fp32 and bf16), compare. Returns (#V index exceptions, #inexact decodes)."""
+    B, H, T, D = k.shape
+    gcache = gpu_encode(k, v, k_bits, k_signed, v_bits, t_cap=t_cap, t_off=t_off)
+    rcache = oracle_encode(k, v, k_bits, k_signed, v_bits, t_cap=t_cap, t_off=t_off)
+    g = cache_to_numpy(gcache)
+    cap = T if t_cap is None else t_cap
+    rows = None
+    if cap != T or t_off:
+        rows = (np.arange(B * H)[:, None] * cap + t_off + np.arange(T)[None, :]).reshape(-1)
+    n_exc = compare_encoded(g, rcache, D, v_bits, v_input=to_oracle(v).reshape(-1, D), rows=rows)
+    # decode the oracle's bytes (tokens [t_off, t_off+T) are what we wrote;
+    # decode reads tokens [0, T_dec) with T_dec = t_off + T)
+    Td = t_off + T
+    inexact = 0
+    dev = cache_from_numpy(rcache)
+    for dt, odt in ((torch.float32, oracle.F32), (torch.bfloat16, oracle.BF16)):
+        kg, vg = tq.tq_decode_kv(dev, Td, k_bits, k_signed, v_bits, out_dtype=dt)
+        torch.cuda.synchronize()
+        kr, vr = oracle.decode_kv(rcache, Td, k_bits, k_signed, v_bits, out_dtype=odt)
+        if dt == torch.float32:
+            inexact += compare_decoded(kg.cpu().numpy(), kr, "K decode")
+            inexact += compare_decoded(vg.cpu().numpy(), vr, "V decode")
+        else:
+            kf, vf = oracle.decode_kv(rcache, Td, k_bits, k_signed, v_bits, out_dtype=oracle.F32)
+            for gt, rt, rf, name in ((kg, kr, kf, "K bf16"), (vg, vr, vf, "V bf16")):
+                gb = gt.cpu().view(torch.int16).numpy().view(np.uint16)
+                if not np.array_equal(gb, rt):
+                    # allowed only where the fp32 results already differ within tolerance
+                    gf = oracle.bf16_bits_to_f32(gb)
+                    rbf = oracle.bf16_bits_to_f32(rt)
+                    nan = np.isnan(rbf)
+                    assert np.array_equal(np.isnan(gf), nan), name
+                    d = np.abs(gf[~nan].astype(np.float64) - rbf[~nan])
+                    assert np.all(d <= 2.0 ** -7 * np.abs(rf[~nan]) + 1e-30), name
+    return n_exc, inexact

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Small shapes cover every (head_dim, value bits, key mode, input dtype)
+combination with ragged row counts that leave a partial last warp step; the
+benchmark workloads run at reduced size element by element, and at full size
+on sampled rows; edge cases cover empty inputs, cache offsets and bytes that
+must stay untouched, and argument errors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import turboquant_kv_cache_tq_gb300 as tq
+from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_append_steps, make_kv, to_oracle
+from tests.gpu_common import (cache_from_numpy, cache_to_numpy, check_roundtrip, compare_decoded,
+                              compare_encoded, gpu_encode, oracle_encode, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+KEY_MODES = [(2, False), (4, False), (5, False), (8, False), (8, True)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _rand(shape, dtype, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(shape, generator=g) * scale
+    return x.to(dtype).contiguous()
+
+
+# ---- every combination, small ragged shapes ---------------------------------------
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+@pytest.mark.parametrize("v_bits", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_all_combinations(D, v_bits, dtype):
+    T = {64: 37, 128: 29, 256: 13, 512: 7}[D]
+    for i, (kb, ks) in enumerate(KEY_MODES):
+        k = _rand((2, 3, T, D), dtype, 100 + i + D + v_bits)
+        v = _rand((2, 3, T, D), dtype, 200 + i + D + v_bits, scale=2.0)
+        n_exc, _ = check_roundtrip(k, v, kb, ks, v_bits)
+        assert n_exc == 0
+
+
+# ---- workloads at reduced size, element by element --------------------------------
+def test_tiny_workload_constant_group():
+    w = WORKLOADS["tiny"]
+    k, v = make_kv(w)
+    for kb, ks in KEY_MODES:
+        check_roundtrip(k, v, kb, ks, 3)
+    g = cache_to_numpy(gpu_encode(k, v, 8, True, 3))
+    # the constant group of K[0,0,0,0:32]: scale 0 and an fp16 +Inf zero point
+    assert g["k_scales"][0, 0, 0, 0] == 0x0000 and g["k_zeros"][0, 0, 0, 0] == 0x7C00
+    kd, _ = tq.tq_decode_kv(cache_from_numpy(g), w.T, 8, True, 3, out_dtype=torch.float32)
+    kd = kd.cpu().numpy()
+    assert np.all(np.isnan(kd[0, 0, 0, :32])) and np.isfinite(kd[0, 0, 0, 32:]).all()
+    assert np.isfinite(kd.reshape(-1, 64)[1:]).all()
+
+
+@pytest.mark.parametrize("name,T", [("llama3_8b_layer", 300), ("hd256", 40), ("hd512", 24), ("long_context", 50)])
+def test_workload_reduced(name, T):
+    w = WORKLOADS[name]
+    B = min(w.B, 3)
+    k, v = make_kv(w, B=B, T=T)
+    for vb in w.v_bits:
+        n_exc, _ = check_roundtrip(k, v, w.k_bits, w.k_signed, vb)
+        assert n_exc == 0
+        # a second key mode on the same data
+        check_roundtrip(k, v, 4, False, vb)
+
+
+# ---- full-size workloads on sampled rows --------------------------------------------
+def _sample_rows(R, n, seed, per_bh=None):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.integers(0, R, n).tolist())
+    rows |= {0, 1, 2, R - 3, R - 2, R - 1}
+    if per_bh:
+        rows |= {i * per_bh for i in range(0, R // per_bh, max(1, R // per_bh // 8))}
+        rows |= {i * per_bh - 1 for i in range(1, R // per_bh, max(1, R // per_bh // 8))}
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_layer", "hd256", "hd512", "long_context"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    k, v = make_kv(w)
+    D = w.D
+    rows = _sample_rows(w.rows, 1500, w.seed, per_bh=w.T)
+    ko = to_oracle(k).reshape(-1, D)[rows].reshape(1, 1, -1, D)
+    vo = to_oracle(v).reshape(-1, D)[rows].reshape(1, 1, -1, D)
+    for vb in w.v_bits:
+        gcache = gpu_encode(k, v, w.k_bits, w.k_signed, vb)
+        ref = oracle.encode_kv(ko, vo, w.k_bits, w.k_signed, vb)
+        g = {key: val.reshape(-1, val.shape[-1])[rows][None, None] for key, val in cache_to_numpy(gcache).items()}
+        compare_encoded(g, ref, D, vb, v_input=vo.reshape(-1, D))
+        # decode at full size, compare the sampled rows with the oracle's decode
+        kd, vd = tq.tq_decode_kv(gcache, w.T, w.k_bits, w.k_signed, vb, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        kr, vr = oracle.decode_kv(ref, len(rows), w.k_bits, w.k_signed, vb)
+        compare_decoded(kd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), kr.reshape(-1, D), "K")
+        compare_decoded(vd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), vr.reshape(-1, D), "V")
+        del gcache, kd, vd
+        torch.cuda.empty_cache()
+
+
+# ---- appends into a preallocated cache ---------------------------------------------
+def test_long_context_appends_equal_one_encode():
+    """The serving mix: a prefix encode into a cache of capacity T + 64, then
+    64 single-token appends at t_off = T + s; the bytes equal one encode of
+    all T + 64 tokens and the oracle's bytes for the same tokens."""
+    w = WORKLOADS["long_context"]
+    B, T = 4, 96
+    k, v = make_kv(w, B=B, T=T)
+    steps = make_append_steps(w)
+    cap = T + len(steps)
+    for vb in w.v_bits:
+        cache = gpu_encode(k, v, w.k_bits, w.k_signed, vb, t_cap=cap)
+        for s, (ks_, vs_) in enumerate(steps):
+            tq.tq_encode_kv(ks_[:B].contiguous().cuda(), vs_[:B].contiguous().cuda(), w.k_bits, w.k_signed, vb,
+                            cache, t_off=T + s)
+        torch.cuda.synchronize()
+        kall = torch.cat([k] + [s_[0][:B] for s_ in steps], dim=2).contiguous()
+        vall = torch.cat([v] + [s_[1][:B] for s_ in steps], dim=2).contiguous()
+        whole = cache_to_numpy(gpu_encode(kall, vall, w.k_bits, w.k_signed, vb))
+        got = cache_to_numpy(cache)
+        for key in got:
+            assert np.array_equal(got[key], whole[key]), key
+        ref = oracle_encode(kall, vall, w.k_bits, w.k_signed, vb)
+        compare_encoded(got, ref, w.D, vb, v_input=to_oracle(vall).reshape(-1, w.D))
+
+
+def test_offsets_touch_only_written_tokens():
+    k = _rand((2, 2, 9, 128), torch.bfloat16, 5)
+    v = _rand((2, 2, 9, 128), torch.bfloat16, 6)
+    cache = gpu_encode(k, v, 8, True, 3, t_cap=16, t_off=5, fill=0xA5)
+    g = cache_to_numpy(cache)
+    ref = oracle_encode(k, v, 8, True, 3, t_cap=16, t_off=5)
+    for key in g:
+        assert np.all(g[key][:, :, :5].view(np.uint8) == 0xA5), key
+        assert np.all(g[key][:, :, 14:].view(np.uint8) == 0xA5), key
+        assert np.array_equal(g[key][:, :, 5:14], ref[key][:, :, 5:14]), key
+    n_exc, _ = check_roundtrip(k, v, 5, False, 5, t_cap=12, t_off=3)
+    assert n_exc == 0
+
+
+def test_decode_leaves_output_padding_untouched():
+    k = _rand((1, 3, 11, 64), torch.bfloat16, 8)
+    v = _rand((1, 3, 11, 64), torch.bfloat16, 9)
+    cache = gpu_encode(k, v, 8, True, 2)
+    big_k = torch.full((1 * 3 * 11 * 64 + 64,), 7.0, dtype=torch.float32, device="cuda")
+    big_v = torch.full_like(big_k, 7.0)
+    ko = big_k[:1 * 3 * 11 * 64].view(1, 3, 11, 64)
+    vo = big_v[:1 * 3 * 11 * 64].view(1, 3, 11, 64)
+    tq.tq_decode_kv(cache, 11, 8, True, 2, out_dtype=torch.float32, k_out=ko, v_out=vo)
+    torch.cuda.synchronize()
+    assert torch.all(big_k[-64:] == 7.0) and torch.all(big_v[-64:] == 7.0)
+
+
+def test_empty_inputs_are_no_ops():
+    cache = tq.alloc_cache(1, 2, 4, 128, 8, 3)
+    for t in cache.values():
+        t.view(torch.uint8).fill_(0x5A)
+    k = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    tq.tq_encode_kv(k, k, 8, True, 3, cache, t_off=4)
+    ko, vo = tq.tq_decode_kv(cache, 0, 8, True, 3)
+    torch.cuda.synchronize()
+    assert ko.numel() == 0 and vo.numel() == 0
+    for t in cache.values():
+        assert torch.all(t.view(torch.uint8) == 0x5A)
+
+
+def test_argument_errors_on_device_tensors():
+    k = torch.zeros((1, 2, 4, 96), dtype=torch.bfloat16, device="cuda")
+    cache = tq.alloc_cache(1, 2, 4, 128, 8, 3)
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_encode_kv(k, k, 8, True, 3, cache)
+    assert e.value.status == 2
+    k = torch.zeros((1, 2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_encode_kv(k, k, 8, True, 6, cache)
+    assert e.value.status == 3
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_encode_kv(k, k, 8, True, 3, cache, t_off=1)
+    assert e.value.status == 1
+    # a K view that starts 2 bytes into its storage: 16-byte alignment fails
+    flat = torch.zeros(1 * 2 * 4 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    kv = flat[1:1 + 1024].view(1, 2, 4, 128)
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_encode_kv(kv, k, 8, True, 3, cache)
+    assert e.value.status == 4
+
+
+# ---- the Lloyd-Max index routine ------------------------------------------------------
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 8])
+def test_lloyd_max_index_at_boundaries(bits):
+    _, b = oracle.lloyd_max(bits)
+    vals = [b]
+    x = b.copy()
+    y = b.copy()
+    for _ in range(4):  # the 4 floats on each side of every boundary
+        x = np.nextafter(x, np.float32(np.inf))
+        y = np.nextafter(y, np.float32(-np.inf))
+        vals += [x.copy(), y.copy()]
+    rng = np.random.default_rng(bits)
+    vals += [rng.standard_normal(200000).astype(np.float32) * 3,
+             rng.uniform(-6, 6, 200000).astype(np.float32),
+             np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e30, -1e30, 5.66, -5.66], np.float32)]
+    # every cell edge of the device's lookup grid and its neighbours
+    grid = {4: (-2.5, 4), 5: (-3.25, 8), 8: (-4.5, 64)}.get(bits)
+    if grid:
+        edges = (grid[0] + np.arange(0, 700) / grid[1]).astype(np.float32)
+        vals += [edges, np.nextafter(edges, np.float32(np.inf)), np.nextafter(edges, np.float32(-np.inf))]
+    u = np.concatenate(vals).astype(np.float32)
+    got = tq.tq_lloyd_max_index(torch.from_numpy(u).cuda(), bits).cpu().numpy()
+    ref = oracle.searchsorted(b, u)
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]

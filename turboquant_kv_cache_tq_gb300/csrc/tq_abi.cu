@@ -84,6 +84,7 @@ tq_status check_common(int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap
   if (bh > 0 && T > lim / bh) return TQ_ERR_INVALID_ARG;
   if (bh > 0 && t_cap > (1LL << 62) / (bh * 512)) return TQ_ERR_INVALID_ARG;
   *rows = bh * T;
+  if (*rows > lim - 64) return TQ_ERR_INVALID_ARG;  // tile arithmetic stays in int
   return TQ_OK;
 }
 
