@@ -41,8 +41,7 @@ def test_all_combinations(D, v_bits, dtype):
     for i, (kb, ks) in enumerate(KEY_MODES):
         k = _rand((2, 3, T, D), dtype, 100 + i + D + v_bits)
         v = _rand((2, 3, T, D), dtype, 200 + i + D + v_bits, scale=2.0)
-        n_exc, _ = check_roundtrip(k, v, kb, ks, v_bits)
-        assert n_exc == 0
+        check_roundtrip(k, v, kb, ks, v_bits)
 
 
 # ---- workloads at reduced size, element by element --------------------------------
@@ -66,8 +65,7 @@ def test_workload_reduced(name, T):
     B = min(w.B, 3)
     k, v = make_kv(w, B=B, T=T)
     for vb in w.v_bits:
-        n_exc, _ = check_roundtrip(k, v, w.k_bits, w.k_signed, vb)
-        assert n_exc == 0
+        check_roundtrip(k, v, w.k_bits, w.k_signed, vb)
         # a second key mode on the same data
         check_roundtrip(k, v, 4, False, vb)
 
@@ -142,8 +140,55 @@ def test_offsets_touch_only_written_tokens():
         assert np.all(g[key][:, :, :5].view(np.uint8) == 0xA5), key
         assert np.all(g[key][:, :, 14:].view(np.uint8) == 0xA5), key
         assert np.array_equal(g[key][:, :, 5:14], ref[key][:, :, 5:14]), key
-    n_exc, _ = check_roundtrip(k, v, 5, False, 5, t_cap=12, t_off=3)
-    assert n_exc == 0
+    check_roundtrip(k, v, 5, False, 5, t_cap=12, t_off=3)
+
+
+def _key_groups(groups, D=64):
+    """A [1,1,T,D] fp32 K tensor whose rows are the given 32-element groups."""
+    g = np.asarray(groups, np.float32).reshape(-1, D)
+    return torch.from_numpy(g.copy()).view(1, 1, -1, D)
+
+
+def test_key_rounding_ties_take_the_exact_path():
+    """Groups whose x / (scale + eps) - zero lands exactly on half-integers:
+    the fast quantisation must hand these to the exact path, which rounds
+    half to even like the page's round()."""
+    half = np.arange(32, dtype=np.float32) + np.float32(0.5)  # 5-bit: scale 1, zero 0, t = i + 0.5
+    sym = np.concatenate([[-127.0, 127.0], np.arange(-15, 15) + 0.5]).astype(np.float32)  # int8: scale 1
+    rows = [np.concatenate([half, half[::-1]]), np.concatenate([sym, -sym]),
+            np.concatenate([half * 2, half - 16])]
+    k = _key_groups(rows)
+    v = torch.from_numpy(np.random.default_rng(0).standard_normal(k.shape).astype(np.float32))
+    for kb, ks in KEY_MODES:
+        check_roundtrip(k, v, kb, ks, 3)
+
+
+def test_key_signed_zero_extremes():
+    """Groups whose min or max is +0 or -0: the zero point keeps the sign of
+    the first such zero in element order, as the page's scan gives."""
+    base = np.abs(np.random.default_rng(1).standard_normal(32)).astype(np.float32) + 0.1
+    rows = []
+    for first, second in ((0.0, -0.0), (-0.0, 0.0)):
+        a = base.copy()
+        a[3], a[17] = first, second  # min is a zero
+        b = -base.copy()
+        b[5], b[29] = first, second  # max is a zero
+        rows += [np.concatenate([a, b])]
+    rows += [np.concatenate([np.full(32, -0.0, np.float32), np.zeros(32, np.float32)])]
+    k = _key_groups(rows)
+    v = torch.from_numpy(np.random.default_rng(2).standard_normal(k.shape).astype(np.float32))
+    for kb, ks in KEY_MODES:
+        check_roundtrip(k, v, kb, ks, 2)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 31, 64, 4097])
+def test_row_to_token_mapping(T):
+    """Rows map to (b*h, t) by a multiply-shift division by T; odd and
+    power-of-two T, with a cache offset, against the oracle."""
+    B, H = 3, 2
+    k = _rand((B, H, T, 128), torch.bfloat16, 40 + T)
+    v = _rand((B, H, T, 128), torch.bfloat16, 41 + T)
+    check_roundtrip(k, v, 8, True, 4, t_cap=T + 5, t_off=2)
 
 
 def test_decode_leaves_output_padding_untouched():
@@ -208,11 +253,10 @@ def test_lloyd_max_index_at_boundaries(bits):
     vals += [rng.standard_normal(200000).astype(np.float32) * 3,
              rng.uniform(-6, 6, 200000).astype(np.float32),
              np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e30, -1e30, 5.66, -5.66], np.float32)]
-    # every cell edge of the device's lookup grid and its neighbours
-    grid = {4: (-2.5, 4), 5: (-3.25, 8), 8: (-4.5, 64)}.get(bits)
-    if grid:
-        edges = (grid[0] + np.arange(0, 700) / grid[1]).astype(np.float32)
-        vals += [edges, np.nextafter(edges, np.float32(np.inf)), np.nextafter(edges, np.float32(-np.inf))]
+    # every cell edge of the device's lookup grid (cells are rint(u * S)) and its neighbours
+    S = {2: 2, 3: 4, 4: 8, 5: 16, 8: 64}[bits]
+    edges = ((np.arange(-8 * S, 8 * S) + 0.5) / S).astype(np.float32)
+    vals += [edges, np.nextafter(edges, np.float32(np.inf)), np.nextafter(edges, np.float32(-np.inf))]
     u = np.concatenate(vals).astype(np.float32)
     got = tq.tq_lloyd_max_index(torch.from_numpy(u).cuda(), bits).cpu().numpy()
     ref = oracle.searchsorted(b, u)

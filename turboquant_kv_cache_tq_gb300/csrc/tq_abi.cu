@@ -29,23 +29,23 @@ int sm_count() {
 namespace {
 
 __global__ void lloyd_max_index_kernel(const float* u, long long n, int v_bits, uint8_t* idx) {
-  __shared__ CellEntry s_cells[CellGrid<8>::n];
-  const CellEntry* tab = v_bits == 4 ? cell_table<4>() : v_bits == 5 ? cell_table<5>() : cell_table<8>();
-  const int nc = v_bits == 4 ? CellGrid<4>::n : v_bits == 5 ? CellGrid<5>::n : CellGrid<8>::n;
-  if (v_bits >= 4) {
-    for (int i = threadIdx.x; i < nc; i += blockDim.x) s_cells[i] = tab[i];
-  }
+  __shared__ CellEntry s_cells[CellGrid<8>::NC];
+  const CellEntry* tab = v_bits == 2 ? cell_table<2>() : v_bits == 3 ? cell_table<3>() : v_bits == 4 ? cell_table<4>()
+                       : v_bits == 5 ? cell_table<5>() : cell_table<8>();
+  const int nc = v_bits == 2 ? CellGrid<2>::NC : v_bits == 3 ? CellGrid<3>::NC : v_bits == 4 ? CellGrid<4>::NC
+               : v_bits == 5 ? CellGrid<5>::NC : CellGrid<8>::NC;
+  for (int i = threadIdx.x; i < nc; i += blockDim.x) s_cells[i] = tab[i];
   __syncthreads();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride) {
     const float x = u[i];
     int r;
     switch (v_bits) {
-      case 2: r = lm_index<2>(x, s_cells); break;
-      case 3: r = lm_index<3>(x, s_cells); break;
-      case 4: r = lm_index<4>(x, s_cells); break;
-      case 5: r = lm_index<5>(x, s_cells); break;
-      default: r = lm_index<8>(x, s_cells); break;
+      case 2: r = lm_index_any<2>(x, s_cells); break;
+      case 3: r = lm_index_any<3>(x, s_cells); break;
+      case 4: r = lm_index_any<4>(x, s_cells); break;
+      case 5: r = lm_index_any<5>(x, s_cells); break;
+      default: r = lm_index_any<8>(x, s_cells); break;
     }
     idx[i] = static_cast<uint8_t>(r);
   }
@@ -132,6 +132,7 @@ extern "C" tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtyp
   p.t_off = t_off;
   p.kmode = key_mode(k_bits, k_signed);
   p.rot_scale = rotation_scale(D);
+  p.tdiv = make_fast_div(static_cast<int>(T));
   const bool bf16 = in_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -172,6 +173,7 @@ extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, con
   p.t_cap = t_cap;
   p.kmode = key_mode(k_bits, k_signed);
   p.rot_scale = rotation_scale(D);
+  p.tdiv = make_fast_div(static_cast<int>(T));
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

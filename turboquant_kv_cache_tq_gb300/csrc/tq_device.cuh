@@ -1,17 +1,23 @@
 // Device building blocks of the TurboQuant codec kernels.
 //
-// Thread layout: every lane holds 8 consecutive head_dim elements of one row
-// (one 16-byte load of bf16). A 32-element quantisation group is 4 adjacent
-// lanes. A row uses D/8 lanes for D <= 256 (so a warp holds 4, 2 or 1 rows);
-// for D = 512 a lane holds two 8-element chunks, at elements 8l and 256 + 8l.
+// Thread layout: lane l of a row owns quantisation group l, i.e. the 32
+// consecutive head_dim elements [32l, 32l+32) of K and of V (one 64-byte
+// load of bf16). A row uses D/32 lanes, so a warp holds 16, 8, 4 or 2 rows
+// for D = 64, 128, 256, 512. Group reductions and the per-group scalars
+// (scale, zero point, reciprocal) stay inside one lane.
 //
-// Rounding contract: every floating-point step is one IEEE binary32 operation
-// with round-to-nearest-even (the __f*_rn intrinsics, rintf, IEEE sqrt and
-// division; this translation unit is built with -fmad=false), taken in the
-// order the codec page applies its ops (page "@mlx-bun/inference 0.0.0-stage
-// -> 1.0.0", file package/src/kernels/turboquant/ops.ts). Reductions whose
-// order is not fixed by the page use one fixed tree (see group_sum_sq and the
-// Hadamard stage order), so the results are deterministic.
+// Pair layout: the 32 fp32 values of a group live in 16 float2 registers,
+// pair p = (element p, element p + 16), so the packed Blackwell fp32x2
+// instructions (__fadd2_rn, __fmul2_rn, __ffma2_rn: two IEEE round-to-nearest
+// operations per instruction) do the butterflies of strides 1..8, the
+// squares and the scalings two elements at a time.
+//
+// Rounding contract: every floating-point step that feeds a stored result is
+// one IEEE binary32 round-to-nearest-even operation in the order the codec
+// page applies its ops (page "@mlx-bun/inference 0.0.0-stage -> 1.0.0", file
+// package/src/kernels/turboquant/ops.ts); a - b is computed as fma(b, -1, a),
+// which is the same single rounding. Reductions whose order the page leaves
+// open use one fixed tree (group_sum_sq, the Hadamard stage order).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -19,6 +25,7 @@
 #include <cstdint>
 #include <limits>
 
+#include "tq_internal.h"
 #include "tq_tables.cuh"
 
 namespace tq {
@@ -26,169 +33,160 @@ namespace tq {
 constexpr int kGroup = 32;     // BLOCK_SIZE on the ops.ts page
 constexpr float kEps = 1e-8f;  // the page's eps as an fp32 scalar
 constexpr unsigned kFull = 0xffffffffu;
+// 1.5 * 2^23: for |t| < 2^22, RN(t + kMagic) = kMagic + rint(t) and the low
+// 22 bits of its encoding hold rint(t) (two's complement around 0x4B400000).
+constexpr float kMagic = 12582912.0f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
 
 template <int D>
 struct Geo {
   static_assert(D == 64 || D == 128 || D == 256 || D == 512, "head_dim");
-  static constexpr int CH = (D == 512) ? 2 : 1;       // 8-element chunks per lane
-  static constexpr int LPR = (D >= 256) ? 32 : D / 8;  // lanes per row
-  static constexpr int RPW = 32 / LPR;                 // rows per warp
+  static constexpr int LPR = D / kGroup;  // lanes per row = groups per row
+  static constexpr int RPW = 32 / LPR;    // rows per warp
 };
 
-// Byte offset, within a packed row of `bits`-bit codes, of the 8 codes of
-// chunk c of lane l (elements c*256 + 8l ... +7).
-template <int BITS>
-__device__ __forceinline__ int chunk_byte(int c, int l) { return (c * 32 + l) * BITS; }
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, f2(-1.0f), a); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// Element offset of chunk c of lane l within a row.
-__device__ __forceinline__ int chunk_elem(int c, int l) { return c * 256 + l * 8; }
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------------------
-// Loads and stores of 8 consecutive elements (16-byte aligned).
-__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {  // bf16 -> fp32 is exact: the high half of the word
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-__device__ __forceinline__ void store8(float* p, const float (&x)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
-}
-
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&x)[8]) {
-  uint32_t w[4];
+// Group loads. A group is 16 words of bf16 pairs (word j = elements 2j, 2j+1)
+// or 32 fp32 values.
+__device__ __forceinline__ void load_words16(const void* p, uint32_t (&w)[16]) {
+  const uint4* q = static_cast<const uint4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-    w[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// ---------------------------------------------------------------------------
-// Rotation: y = H x / sqrt(D) (Sylvester order) for the row held by the LPR
-// lanes of this row. Radix-2 stages in ascending stride: 1, 2, 4 inside a
-// chunk, 8 .. 8*(LPR/2) across lanes (xor shuffles), then 256 across the two
-// chunks of D = 512. Stage h maps (a, b) = (x[i], x[i+h]) to (a + b, a - b).
-// The cross-lane update x' = fma(x, s, partner) with s = +1 (lower lane) or
-// -1 (upper lane) is exactly one rounded add or subtract.
-template <int D>
-__device__ __forceinline__ void hadamard_unnormalised(float (&x)[Geo<D>::CH][8], int l) {
-  constexpr int CH = Geo<D>::CH;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if ((i & h) == 0) {
-          const float a = x[c][i], b = x[c][i + h];
-          x[c][i] = __fadd_rn(a, b);
-          x[c][i + h] = __fsub_rn(a, b);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int m = 1; m < Geo<D>::LPR; m <<= 1) {
-    const float s = (l & m) ? -1.0f : 1.0f;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p = __shfl_xor_sync(kFull, x[c][i], m);
-        x[c][i] = __fmaf_rn(x[c][i], s, p);
-      }
-    }
-  }
-  if constexpr (CH == 2) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float a = x[0][i], b = x[1][i];
-      x[0][i] = __fadd_rn(a, b);
-      x[1][i] = __fsub_rn(a, b);
-    }
+    const uint4 u = __ldg(q + i);
+    w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
   }
 }
 
-// Multiply by -1 where the sign table says so (exact: flips the sign bit).
-__device__ __forceinline__ void apply_signs(float (&x)[8], uint32_t neg_bits) {
+__device__ __forceinline__ void load_floats32(const float* p, float (&x)[32]) {
+  const float4* q = reinterpret_cast<const float4*>(p);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    x[i] = __uint_as_float(__float_as_uint(x[i]) ^ (((neg_bits >> i) & 1u) << 31));
+    const float4 u = __ldg(q + i);
+    x[4 * i] = u.x; x[4 * i + 1] = u.y; x[4 * i + 2] = u.z; x[4 * i + 3] = u.w;
   }
+}
+
+// bf16 words -> pairs (element p, element p + 16)
+__device__ __forceinline__ void words_to_pairs(const uint32_t (&w)[16], float2 (&P)[16]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    P[2 * j] = make_float2(bf16_lo(w[j]), bf16_lo(w[j + 8]));
+    P[2 * j + 1] = make_float2(bf16_hi(w[j]), bf16_hi(w[j + 8]));
+  }
+}
+
+__device__ __forceinline__ void floats_to_pairs(const float (&x)[32], float2 (&P)[16]) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p) P[p] = make_float2(x[p], x[p + 16]);
+}
+
+// Element i of a pair array.
+__device__ __forceinline__ float pair_elem(const float2 (&P)[16], int i) { return i < 16 ? P[i].x : P[i - 16].y; }
+
+// Sign words: word j of a group has bit 15 set when element 2j has sign -1
+// and bit 31 set when element 2j + 1 has; XOR into a bf16 pair word negates.
+// A block keeps the D/2 words of its head_dim in shared memory.
+template <int D>
+__device__ __forceinline__ uint32_t sign_word(int l, int j) {
+  const uint8_t* t;
+  if constexpr (D == 64) t = kSignNeg64;
+  else if constexpr (D == 128) t = kSignNeg128;
+  else if constexpr (D == 256) t = kSignNeg256;
+  else t = kSignNeg512;
+  const int e = 32 * l + 2 * j;  // element index of the low half
+  const uint32_t b = t[e >> 3];
+  return (((b >> (e & 7)) & 1u) << 15) | (((b >> ((e & 7) + 1)) & 1u) << 31);
 }
 
 template <int D>
-__device__ __forceinline__ uint32_t sign_byte(int idx) {
-  if constexpr (D == 64) return kSignNeg64[idx];
-  else if constexpr (D == 128) return kSignNeg128[idx];
-  else if constexpr (D == 256) return kSignNeg256[idx];
-  else return kSignNeg512[idx];
+__device__ __forceinline__ void fill_sign_words(uint32_t* s_sign) {
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) s_sign[i] = sign_word<D>(i / 16, i % 16);
 }
 
-// ---------------------------------------------------------------------------
-// Group reductions over the 4 lanes (32 elements) of a quantisation group.
-
-// Min and max with the tie rule of a left-to-right scan (the first of equal
-// values wins, which only matters for +0 / -0): in-lane in element order,
-// then across lanes preferring the lower lane.
-__device__ __forceinline__ void group_min_max(const float (&x)[8], int l, float& mn, float& mx) {
-  mn = x[0];
-  mx = x[0];
+// The 16 sign words of group l.
+__device__ __forceinline__ void load_sign_words(const uint32_t* s_sign, int l, uint32_t (&S)[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(s_sign + 16 * l);
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    mn = (x[i] < mn) ? x[i] : mn;
-    mx = (x[i] > mx) ? x[i] : mx;
-  }
-#pragma unroll
-  for (int m = 1; m <= 2; m <<= 1) {
-    const float omn = __shfl_xor_sync(kFull, mn, m);
-    const float omx = __shfl_xor_sync(kFull, mx, m);
-    const bool partner_lower = (l & m) != 0;
-    mn = (omn < mn || (omn == mn && partner_lower)) ? omn : mn;
-    mx = (omx > mx || (omx == mx && partner_lower)) ? omx : mx;
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = q[i];
+    S[4 * i] = u.x; S[4 * i + 1] = u.y; S[4 * i + 2] = u.z; S[4 * i + 3] = u.w;
   }
 }
 
-// Sum of squares of the group's 32 elements as a pairwise tree: within a lane
-// ((0,1),(2,3)),((4,5),(6,7)); then lanes (0,1),(2,3); then the two halves.
-// Addition is commutative in IEEE arithmetic, so all 4 lanes get equal bits.
-__device__ __forceinline__ float group_sum_sq(const float (&y)[8]) {
-  float q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(y[i], y[i]);
-  const float s01 = __fadd_rn(q[0], q[1]), s23 = __fadd_rn(q[2], q[3]);
-  const float s45 = __fadd_rn(q[4], q[5]), s67 = __fadd_rn(q[6], q[7]);
-  float s = __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
-  s = __fadd_rn(s, __shfl_xor_sync(kFull, s, 1));
-  s = __fadd_rn(s, __shfl_xor_sync(kFull, s, 2));
-  return s;
+// Sign bit (bit 31) of element i of the group, from the sign words.
+__device__ __forceinline__ uint32_t elem_sign(const uint32_t (&S)[16], int i) {
+  return (i & 1) ? (S[i >> 1] & 0x80000000u) : ((S[i >> 1] << 16) & 0x80000000u);
 }
 
 // ---------------------------------------------------------------------------
-// Lloyd-Max index = count(boundaries < u) (ops.ts, searchsorted).
-//
-// 2 and 3 bits: compare against the 3 or 7 boundaries as immediates.
-// 4, 5, 8 bits: a cell table. cell(u) = clamp(floor((u - lo) * 2^k), 0, n-1)
-// is monotone in u, so every boundary in a lower cell than u is below u and
-// every boundary in a higher cell is at or above u; each cell holds at most
-// one boundary (the grid step is below the table's smallest boundary gap),
-// which is compared explicitly. The table is built at compile time with the
-// same two fp32 operations (the product by 2^k is exact) and checked against
-// the plain count by the tests on values at and next to every boundary.
+// Rotation: H x (Sylvester order, unnormalised) on the D elements of a row
+// held by its LPR lanes. Radix-2 stages in ascending stride: 1, 2, 4, 8 as
+// packed ops across pairs, 16 inside each pair, then 32 .. D/2 across lanes
+// (xor shuffles). Stage h maps (a, b) = (x[i], x[i+h]) to (a + b, a - b);
+// across lanes the update is fma(x, s, partner), s = +1 in the lower lane
+// and -1 in the upper one, i.e. exactly partner + x or partner - x.
+template <int LPR>
+__device__ __forceinline__ void hadamard_row(float2 (&P)[16], int l) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      if ((p & h) == 0) {
+        const float2 a = P[p], b = P[p + h];
+        P[p] = add2(a, b);
+        P[p + h] = sub2(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const float a = P[p].x, b = P[p].y;
+    P[p] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+  }
+#pragma unroll
+  for (int m = 1; m < LPR; m <<= 1) {
+    const float2 s = f2((l & m) ? -1.0f : 1.0f);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const float2 q = make_float2(__shfl_xor_sync(kFull, P[p].x, m), __shfl_xor_sync(kFull, P[p].y, m));
+      P[p] = fma2(P[p], s, q);
+    }
+  }
+}
+
+// Sum of squares of a group as the pairwise tree over elements 0..31 in
+// index order: (0,1),(2,3),... then pairs of those, up to (0..15)+(16..31).
+__device__ __forceinline__ float group_sum_sq(const float2 (&P)[16]) {
+  float2 q[16];
+#pragma unroll
+  for (int p = 0; p < 16; ++p) q[p] = mul2(P[p], P[p]);
+#pragma unroll
+  for (int w = 1; w < 16; w <<= 1) {
+#pragma unroll
+    for (int p = 0; p < 16; p += 2 * w) q[p] = add2(q[p], q[p + w]);
+  }
+  return __fadd_rn(q[0].x, q[0].y);
+}
+
+// ---------------------------------------------------------------------------
+// Lloyd-Max index = count(boundaries < u) (ops.ts, searchsorted), via a cell
+// table. cell(u) = rint(u * S) + OFF with S a power of two, computed as the
+// low bits of RN(u * S + (1.5 * 2^23 + OFF)) (u * S is exact, so this is one
+// rounding on the device and in the compile-time builder alike). cell() is
+// monotone, so a boundary in a lower cell than u is below u and one in a
+// higher cell is not; each cell holds at most one boundary (the cell width
+// 1/S is below the table's smallest boundary gap), compared explicitly: u > b
+// exactly when RN(b - u) has its sign bit set. The grid covers |u| < 7.9; for
+// finite inputs |u| <= sqrt(32) since u is a coordinate over its group's RMS.
 struct CellEntry {
   float b;   // the boundary inside this cell, or +Inf
   int base;  // number of boundaries in lower cells
@@ -196,21 +194,11 @@ struct CellEntry {
 
 template <int BITS>
 struct CellGrid;
-template <>
-struct CellGrid<4> {
-  static constexpr float lo = -2.5f, scale = 4.0f;
-  static constexpr int n = 20;
-};
-template <>
-struct CellGrid<5> {
-  static constexpr float lo = -3.25f, scale = 8.0f;
-  static constexpr int n = 52;
-};
-template <>
-struct CellGrid<8> {
-  static constexpr float lo = -4.5f, scale = 64.0f;
-  static constexpr int n = 576;
-};
+template <> struct CellGrid<2> { static constexpr float S = 2.0f;  static constexpr int NC = 32, OFF = 16; };
+template <> struct CellGrid<3> { static constexpr float S = 4.0f;  static constexpr int NC = 64, OFF = 32; };
+template <> struct CellGrid<4> { static constexpr float S = 8.0f;  static constexpr int NC = 128, OFF = 64; };
+template <> struct CellGrid<5> { static constexpr float S = 16.0f; static constexpr int NC = 256, OFF = 128; };
+template <> struct CellGrid<8> { static constexpr float S = 64.0f; static constexpr int NC = 1024, OFF = 512; };
 
 template <int N>
 struct CellTable {
@@ -226,40 +214,45 @@ __host__ __device__ constexpr float lm_boundary(int j) {
   else return LloydMax8::boundary(j);
 }
 
-// Cell of u on the grid of a table, in the same two fp32 operations the
-// device uses (the product by a power of two is exact).
 template <int BITS>
-constexpr int grid_cell(float u) {
-  const float d = u - CellGrid<BITS>::lo;  // one fp32 rounding
-  const float s = d * CellGrid<BITS>::scale;
-  return static_cast<int>(s);
+constexpr float grid_magic() {
+  return kMagic + static_cast<float>(CellGrid<BITS>::OFF);
 }
 
-// True when every boundary lies inside the grid and no cell holds two.
+// The cell of u, with the device's arithmetic (one rounding of an exact
+// product plus a constant); bounds are the caller's business.
+template <int BITS>
+constexpr int grid_cell_host(float u) {
+  const float prod = u * CellGrid<BITS>::S;  // exact: S is a power of two
+  const float s = prod + grid_magic<BITS>();  // one rounding
+  return static_cast<int>(static_cast<long long>(s) - static_cast<long long>(kMagic));
+}
+
 template <int BITS>
 constexpr bool cell_grid_fits() {
   int prev = -1;
   for (int j = 0; j < (1 << BITS) - 1; ++j) {
     const float b = lm_boundary<BITS>(j);
-    if (b < CellGrid<BITS>::lo) return false;
-    const int c = grid_cell<BITS>(b);
-    if (c <= prev || c >= CellGrid<BITS>::n) return false;
+    if (b < -7.0f || b > 7.0f) return false;
+    const int c = grid_cell_host<BITS>(b);
+    if (c <= prev || c < 0 || c >= CellGrid<BITS>::NC) return false;
     prev = c;
   }
   return true;
 }
-static_assert(cell_grid_fits<4>() && cell_grid_fits<5>() && cell_grid_fits<8>(),
+static_assert(cell_grid_fits<2>() && cell_grid_fits<3>() && cell_grid_fits<4>() && cell_grid_fits<5>() &&
+                  cell_grid_fits<8>(),
               "a Lloyd-Max cell grid is too coarse for its table");
 
 template <int BITS>
-constexpr CellTable<CellGrid<BITS>::n> make_cell_table() {
-  constexpr int n = CellGrid<BITS>::n;
+constexpr CellTable<CellGrid<BITS>::NC> make_cell_table() {
+  constexpr int n = CellGrid<BITS>::NC;
   CellTable<n> t{};
   for (int c = 0; c < n; ++c) {
     t.e[c].b = std::numeric_limits<float>::infinity();
     t.e[c].base = 0;
   }
-  for (int j = 0; j < (1 << BITS) - 1; ++j) t.e[grid_cell<BITS>(lm_boundary<BITS>(j))].b = lm_boundary<BITS>(j);
+  for (int j = 0; j < (1 << BITS) - 1; ++j) t.e[grid_cell_host<BITS>(lm_boundary<BITS>(j))].b = lm_boundary<BITS>(j);
   int count = 0;
   for (int c = 0; c < n; ++c) {
     t.e[c].base = count;
@@ -268,38 +261,41 @@ constexpr CellTable<CellGrid<BITS>::n> make_cell_table() {
   return t;
 }
 
-__device__ const CellTable<CellGrid<4>::n> kCells4 = make_cell_table<4>();
-__device__ const CellTable<CellGrid<5>::n> kCells5 = make_cell_table<5>();
-__device__ const CellTable<CellGrid<8>::n> kCells8 = make_cell_table<8>();
+__device__ const CellTable<CellGrid<2>::NC> kCells2 = make_cell_table<2>();
+__device__ const CellTable<CellGrid<3>::NC> kCells3 = make_cell_table<3>();
+__device__ const CellTable<CellGrid<4>::NC> kCells4 = make_cell_table<4>();
+__device__ const CellTable<CellGrid<5>::NC> kCells5 = make_cell_table<5>();
+__device__ const CellTable<CellGrid<8>::NC> kCells8 = make_cell_table<8>();
 
 template <int BITS>
 __device__ __forceinline__ const CellEntry* cell_table() {
-  if constexpr (BITS == 4) return kCells4.e;
+  if constexpr (BITS == 2) return kCells2.e;
+  else if constexpr (BITS == 3) return kCells3.e;
+  else if constexpr (BITS == 4) return kCells4.e;
   else if constexpr (BITS == 5) return kCells5.e;
   else return kCells8.e;
 }
 
+// Indices of a pair of values (finite, |u| < 7.9) from the table in shared memory.
 template <int BITS>
-__device__ __forceinline__ int lm_index_cells(float u, const CellEntry* tab) {
+__device__ __forceinline__ void lm_index2(float2 u, const CellEntry* tab, int& i0, int& i1) {
   using G = CellGrid<BITS>;
-  float s = __fmul_rn(__fsub_rn(u, G::lo), G::scale);
-  s = fminf(fmaxf(s, 0.0f), static_cast<float>(G::n - 1));  // NaN -> 0
-  const CellEntry e = tab[static_cast<int>(s)];
-  return e.base + (u > e.b ? 1 : 0);
+  const float2 s = fma2(u, f2(G::S), f2(grid_magic<BITS>()));
+  const CellEntry e0 = tab[__float_as_uint(s.x) & (G::NC - 1)];
+  const CellEntry e1 = tab[__float_as_uint(s.y) & (G::NC - 1)];
+  const float2 d = sub2(make_float2(e0.b, e1.b), u);  // RN(b - u) < 0 exactly when u > b
+  i0 = e0.base + static_cast<int>(__float_as_uint(d.x) >> 31);
+  i1 = e1.base + static_cast<int>(__float_as_uint(d.y) >> 31);
 }
 
+// Any fp32 value: clamp into the grid first (all boundaries lie inside it, so
+// the count is unchanged; NaN clamps to the low end and counts nothing).
 template <int BITS>
-__device__ __forceinline__ int lm_index_direct(float u) {
-  int idx = 0;
-#pragma unroll
-  for (int j = 0; j < (1 << BITS) - 1; ++j) idx += (u > lm_boundary<BITS>(j)) ? 1 : 0;
-  return idx;
-}
-
-template <int BITS>
-__device__ __forceinline__ int lm_index(float u, const CellEntry* tab) {
-  if constexpr (BITS <= 3) return lm_index_direct<BITS>(u);
-  else return lm_index_cells<BITS>(u, tab);
+__device__ __forceinline__ int lm_index_any(float u, const CellEntry* tab) {
+  const float c = fminf(fmaxf(u, -7.5f), 7.5f);
+  int i0, i1;
+  lm_index2<BITS>(make_float2(c, c), tab, i0, i1);
+  return i0;
 }
 
 template <int BITS>
@@ -313,50 +309,73 @@ __device__ __forceinline__ const float* centroid_table() {
 
 // ---------------------------------------------------------------------------
 // Bit packing (ops.ts, packBits / unpackBits): code i of a row occupies bits
-// [i*b, i*b+b) of a little-endian bitstream, so the 8 codes of a chunk fill
-// exactly b bytes starting at byte chunk*b.
-template <int BITS>
-__device__ __forceinline__ uint64_t pack8(const int (&q)[8]) {
-  uint64_t acc = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc |= static_cast<uint64_t>(q[i] & ((1 << BITS) - 1)) << (i * BITS);
-  return acc;
+// [i*b, i*b+b) of a little-endian bitstream, so the 32 codes of group l fill
+// exactly b 32-bit words starting at byte 4*b*l of the packed row.
+// OR code i (its low B bits) into its place in the packed words.
+template <int B>
+__device__ __forceinline__ void put_code(uint32_t (&w)[B], int i, uint32_t c) {
+  const uint32_t v = c & ((1u << B) - 1u);
+  const int bit = i * B, word = bit >> 5, off = bit & 31;
+  w[word] |= v << off;
+  if (off + B > 32) w[word + 1] |= v >> (32 - off);
 }
 
-template <int BITS>
-__device__ __forceinline__ void store_packed(uint8_t* p, uint64_t acc) {
-  if constexpr (BITS == 8) {
-    *reinterpret_cast<uint2*>(p) = make_uint2(static_cast<uint32_t>(acc), static_cast<uint32_t>(acc >> 32));
-  } else if constexpr (BITS == 4) {
-    *reinterpret_cast<uint32_t*>(p) = static_cast<uint32_t>(acc);
-  } else if constexpr (BITS == 2) {
-    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(acc);
+template <int B>
+__device__ __forceinline__ uint32_t unpack_code(const uint32_t (&w)[B], int i) {
+  const int bit = i * B, word = bit >> 5, off = bit & 31;
+  uint32_t v = w[word] >> off;
+  if (off + B > 32) v |= w[word + 1] << (32 - off);
+  return v & ((1u << B) - 1u);
+}
+
+template <int B>
+__device__ __forceinline__ void store_words(uint8_t* p, const uint32_t (&w)[B]) {
+  if constexpr (B == 8) {
+    reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else if constexpr (B == 4) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (B == 2) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
   } else {
 #pragma unroll
-    for (int i = 0; i < BITS; ++i) p[i] = static_cast<uint8_t>(acc >> (8 * i));
+    for (int k = 0; k < B; ++k) reinterpret_cast<uint32_t*>(p)[k] = w[k];
   }
 }
 
-template <int BITS>
-__device__ __forceinline__ uint64_t load_packed(const uint8_t* p) {
-  if constexpr (BITS == 8) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-    return static_cast<uint64_t>(u.x) | (static_cast<uint64_t>(u.y) << 32);
-  } else if constexpr (BITS == 4) {
-    return __ldg(reinterpret_cast<const uint32_t*>(p));
-  } else if constexpr (BITS == 2) {
-    return __ldg(reinterpret_cast<const uint16_t*>(p));
+template <int B>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[B]) {
+  if constexpr (B == 8) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else if constexpr (B == 4) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  } else if constexpr (B == 2) {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+    w[0] = a.x; w[1] = a.y;
   } else {
-    uint64_t acc = 0;
 #pragma unroll
-    for (int i = 0; i < BITS; ++i) acc |= static_cast<uint64_t>(__ldg(p + i)) << (8 * i);
-    return acc;
+    for (int k = 0; k < B; ++k) w[k] = __ldg(reinterpret_cast<const uint32_t*>(p) + k);
   }
 }
 
-template <int BITS>
-__device__ __forceinline__ int unpack_code(uint64_t acc, int i) {
-  return static_cast<int>((acc >> (i * BITS)) & ((1u << BITS) - 1));
+// ---------------------------------------------------------------------------
+// Row -> (b*h, t) by a multiply-shift: for 0 <= r < 2^31 and 1 <= T < 2^31,
+// with s = ceil(log2 T) and m = ceil(2^(32+s) / T), floor(r * m / 2^(32+s))
+// equals floor(r / T) (the error term r * (m*T - 2^(32+s)) / (T * 2^(32+s))
+// stays below 1/(2T)).
+__host__ inline FastDiv make_fast_div(int T) {
+  int s = 0;
+  while ((1LL << s) < T) ++s;
+  const unsigned __int128 num = static_cast<unsigned __int128>(1) << (32 + s);
+  const unsigned long long m = static_cast<unsigned long long>((num + T - 1) / T);
+  return FastDiv{m, 32 + s};
+}
+
+__device__ __forceinline__ int fast_div(int r, FastDiv d) {
+  return static_cast<int>((static_cast<unsigned long long>(r) * d.m) >> d.shift);
 }
 
 }  // namespace tq

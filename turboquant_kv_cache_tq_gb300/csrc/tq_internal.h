@@ -7,6 +7,12 @@
 
 namespace tq {
 
+// Row -> (b*h, t) by a multiply-shift (see fast_div in tq_device.cuh).
+struct FastDiv {
+  unsigned long long m;
+  int shift;
+};
+
 // Key modes: (bits, signed) pairs the key path supports.
 enum KeyMode : int { kK2 = 0, kK4 = 1, kK5 = 2, kK8 = 3, kK8Signed = 4 };
 
@@ -24,6 +30,7 @@ struct EncodeParams {
   long long t_off;      // first cache token written
   int kmode;            // KeyMode
   float rot_scale;      // fp32(1/sqrt(D))
+  FastDiv tdiv;         // division by T
 };
 
 struct DecodeParams {
@@ -39,6 +46,7 @@ struct DecodeParams {
   long long t_cap;
   int kmode;
   float rot_scale;
+  FastDiv tdiv;
 };
 
 // One launcher per head_dim (tq_kernels_d<D>.cu); v_bits in {2,3,4,5,8}.
