@@ -133,6 +133,7 @@ extern "C" tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtyp
   p.kmode = key_mode(k_bits, k_signed);
   p.rot_scale = rotation_scale(D);
   p.tdiv = make_fast_div(static_cast<int>(T));
+  p.neg_zero = -0.0f;
   const bool bf16 = in_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -174,6 +175,7 @@ extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, con
   p.kmode = key_mode(k_bits, k_signed);
   p.rot_scale = rotation_scale(D);
   p.tdiv = make_fast_div(static_cast<int>(T));
+  p.neg_zero = -0.0f;
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

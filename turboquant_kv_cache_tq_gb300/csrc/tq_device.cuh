@@ -8,9 +8,9 @@
 //
 // Pair layout: the 32 fp32 values of a group live in 16 float2 registers,
 // pair p = (element p, element p + 16), so the packed Blackwell fp32x2
-// instructions (__fadd2_rn, __fmul2_rn, __ffma2_rn: two IEEE round-to-nearest
-// operations per instruction) do the butterflies of strides 1..8, the
-// squares and the scalings two elements at a time.
+// instructions (add/mul/fma.rn.f32x2: two IEEE round-to-nearest operations
+// per instruction) do the butterflies of strides 1..8, the squares and the
+// scalings two elements at a time.
 //
 // Rounding contract: every floating-point step that feeds a stored result is
 // one IEEE binary32 round-to-nearest-even operation in the order the codec
@@ -45,11 +45,40 @@ struct Geo {
   static constexpr int RPW = 32 / LPR;    // rows per warp
 };
 
+// Packed fp32x2 operations (PTX add/mul/fma.rn.f32x2), each component one IEEE
+// round-to-nearest-even operation. The code generator may still fuse a packed
+// multiply into a packed add that consumes it (measured on sm_103a even with
+// explicit .rn modifiers), which would skip the product's rounding. So every
+// product that feeds an add is formed as mul0(a, b, z) = fma(a, b, z) with z a
+// runtime -0.0 from the kernel arguments: a*b + (-0) rounds to exactly
+// RN(a*b) for every a, b (including signed zeros), and an fma result is never
+// fused further.
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, f2(-1.0f), a); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+// a - b as fma(b, -1, a): one rounding of the exact difference
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return fma2(b, f2(-1.0f), a); }
+// RN(a * b) that cannot be fused into a consumer; nz must hold a runtime -0.0
+__device__ __forceinline__ float2 mul0(float2 a, float2 b, float2 nz) { return fma2(a, b, nz); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -165,10 +194,10 @@ __device__ __forceinline__ void hadamard_row(float2 (&P)[16], int l) {
 
 // Sum of squares of a group as the pairwise tree over elements 0..31 in
 // index order: (0,1),(2,3),... then pairs of those, up to (0..15)+(16..31).
-__device__ __forceinline__ float group_sum_sq(const float2 (&P)[16]) {
+__device__ __forceinline__ float group_sum_sq(const float2 (&P)[16], float2 nz) {
   float2 q[16];
 #pragma unroll
-  for (int p = 0; p < 16; ++p) q[p] = mul2(P[p], P[p]);
+  for (int p = 0; p < 16; ++p) q[p] = mul0(P[p], P[p], nz);
 #pragma unroll
   for (int w = 1; w < 16; w <<= 1) {
 #pragma unroll
@@ -276,7 +305,8 @@ __device__ __forceinline__ const CellEntry* cell_table() {
   else return kCells8.e;
 }
 
-// Indices of a pair of values (finite, |u| < 7.9) from the table in shared memory.
+// Indices of a pair of values (finite, |u| < 7.9) from the table in shared
+// memory; u must not be an unfused product (see mul0).
 template <int BITS>
 __device__ __forceinline__ void lm_index2(float2 u, const CellEntry* tab, int& i0, int& i1) {
   using G = CellGrid<BITS>;

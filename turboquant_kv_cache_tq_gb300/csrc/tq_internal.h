@@ -31,6 +31,7 @@ struct EncodeParams {
   int kmode;            // KeyMode
   float rot_scale;      // fp32(1/sqrt(D))
   FastDiv tdiv;         // division by T
+  float neg_zero;       // -0.0f (a runtime value, see mul0)
 };
 
 struct DecodeParams {
@@ -47,6 +48,7 @@ struct DecodeParams {
   int kmode;
   float rot_scale;
   FastDiv tdiv;
+  float neg_zero;       // -0.0f
 };
 
 // One launcher per head_dim (tq_kernels_d<D>.cu); v_bits in {2,3,4,5,8}.

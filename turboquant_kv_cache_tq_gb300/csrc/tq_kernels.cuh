@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
       const float2 c2 = f2(p.rot_scale);
 #pragma unroll
       for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
-      const float rms = __fsqrt_rn(__fmul_rn(group_sum_sq(Y), 1.0f / kGroup));  // /32 is exact
+      const float2 nz = f2(p.neg_zero);
+      const float rms = __fsqrt_rn(__fmul_rn(group_sum_sq(Y, nz), 1.0f / kGroup));  // /32 is exact
       const float inv = __frcp_rn(__fadd_rn(rms, kEps));
       uint32_t w[VB];
 #pragma unroll
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         int i0, i1;
-        lm_index2<VB>(mul2(Y[q], f2(inv)), s_cells, i0, i1);
+        lm_index2<VB>(mul0(Y[q], f2(inv), nz), s_cells, i0, i1);
         put_code<VB>(w, q, static_cast<uint32_t>(i0));
         put_code<VB>(w, q + 16, static_cast<uint32_t>(i1));
       }
@@ -335,10 +336,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       load_words<VB>(p.v_codes + irow * pdv + 4 * VB * l, w);
       const float s = __half2float(__ushort_as_half(__ldg(p.v_scales + irow * NG + l)));
       float2 Y[16];
+      const float2 nz = f2(p.neg_zero);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const float2 c = make_float2(s_cent[unpack_code<VB>(w, q)], s_cent[unpack_code<VB>(w, q + 16)]);
-        Y[q] = mul2(c, f2(s));
+        Y[q] = mul0(c, f2(s), nz);  // feeds the butterflies: must stay rounded
       }
       hadamard_row<G::LPR>(Y, l);
       const float2 c2 = f2(p.rot_scale);
