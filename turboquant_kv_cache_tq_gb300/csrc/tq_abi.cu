@@ -172,6 +172,9 @@ extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, con
   p.rows = static_cast<int>(rows);
   p.T = static_cast<int>(T);
   p.t_cap = t_cap;
+  p.pdk = static_cast<int>(D * k_bits / 8);
+  p.pdv = static_cast<int>(D * v_bits / 8);
+  p.ng = static_cast<int>(D / 32);
   p.kmode = key_mode(k_bits, k_signed);
   p.rot_scale = rotation_scale(D);
   p.tdiv = make_fast_div(static_cast<int>(T));

@@ -318,6 +318,21 @@ __device__ __forceinline__ void lm_index2(float2 u, const CellEntry* tab, int& i
   i1 = e1.base + static_cast<int>(__float_as_uint(d.y) >> 31);
 }
 
+// Indices of the pair y * inv without rounding the product first: the cell
+// is RN(y * (inv * S) + magic) (inv * S is exact) and the comparison is the
+// sign of RN(b - y * inv) (one fma), so both use the same exact value
+// v = y * inv and the result is exactly count(boundaries < v).
+template <int BITS>
+__device__ __forceinline__ void lm_index2_scaled(float2 y, float inv, const CellEntry* tab, int& i0, int& i1) {
+  using G = CellGrid<BITS>;
+  const float2 s = fma2(y, f2(__fmul_rn(inv, G::S)), f2(grid_magic<BITS>()));
+  const CellEntry e0 = tab[__float_as_uint(s.x) & (G::NC - 1)];
+  const CellEntry e1 = tab[__float_as_uint(s.y) & (G::NC - 1)];
+  const float2 d = fma2(y, f2(-inv), make_float2(e0.b, e1.b));
+  i0 = e0.base + static_cast<int>(__float_as_uint(d.x) >> 31);
+  i1 = e1.base + static_cast<int>(__float_as_uint(d.y) >> 31);
+}
+
 // Any fp32 value: clamp into the grid first (all boundaries lie inside it, so
 // the count is unchanged; NaN clamps to the low end and counts nothing).
 template <int BITS>
@@ -341,13 +356,23 @@ __device__ __forceinline__ const float* centroid_table() {
 // Bit packing (ops.ts, packBits / unpackBits): code i of a row occupies bits
 // [i*b, i*b+b) of a little-endian bitstream, so the 32 codes of group l fill
 // exactly b 32-bit words starting at byte 4*b*l of the packed row.
-// OR code i (its low B bits) into its place in the packed words.
+// Put code i (its low B bits) into its place in the packed words. The words
+// start at zero and every code owns its own bits, so the shifted code can be
+// added (one shift-add instruction) instead of masked and or-ed in.
 template <int B>
 __device__ __forceinline__ void put_code(uint32_t (&w)[B], int i, uint32_t c) {
   const uint32_t v = c & ((1u << B) - 1u);
   const int bit = i * B, word = bit >> 5, off = bit & 31;
-  w[word] |= v << off;
-  if (off + B > 32) w[word + 1] |= v >> (32 - off);
+  w[word] += v << off;
+  if (off + B > 32) w[word + 1] += v >> (32 - off);
+}
+
+// The same for a code already known to fit in B bits (no mask).
+template <int B>
+__device__ __forceinline__ void put_code_exact(uint32_t (&w)[B], int i, uint32_t v) {
+  const int bit = i * B, word = bit >> 5, off = bit & 31;
+  w[word] += v << off;
+  if (off + B > 32) w[word + 1] += v >> (32 - off);
 }
 
 template <int B>

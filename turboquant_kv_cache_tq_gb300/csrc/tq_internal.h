@@ -49,6 +49,8 @@ struct DecodeParams {
   float rot_scale;
   FastDiv tdiv;
   float neg_zero;       // -0.0f
+  int pdk, pdv;         // bytes of a packed K / V row
+  int ng;               // groups per row (D / 32)
 };
 
 // One launcher per head_dim (tq_kernels_d<D>.cu); v_bits in {2,3,4,5,8}.

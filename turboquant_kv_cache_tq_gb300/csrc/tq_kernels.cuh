@@ -17,14 +17,24 @@
 //      is farther than that from a half-integer both round to the same code.
 //      A lane whose group has any element inside that band recomputes the
 //      group with IEEE division; K codes are therefore exactly the page's.
-//   V: u = RN(y * RN(1/se)) is within 2 ulp of RN(y / se) (|u| <= sqrt(32),
-//      so within 1.1e-6); an index can only differ from the divided value's
-//      when u is that close to a boundary.
+//   V: the index is count(boundaries < v) for the exact product
+//      v = y * RN(1/se), which is within one ulp of RN(y / se) (|v| <=
+//      sqrt(32), so within 5e-7); it can only differ from the divided value's
+//      index when v is that close to a boundary.
 //
-// One warp handles Geo<D>::RPW rows per step of a grid-stride loop over all
-// B*H*T rows; the grid is sized to the resident capacity of the GPU. Lanes of
-// a partial last step redo the last row (so shuffles stay converged) but
-// store nothing.
+// Work split: a work item is the K half or the V half of a tile of
+// Geo<D>::RPW rows. Item `it` maps to tile it/2, and a warp alternates kinds
+// from one grid-stride step to the next (kind = (it ^ step) & 1, a bijection
+// because the number of warps is even), so registers cover one half at a time
+// and blocks stay balanced. The next item's inputs are loaded before the
+// current item's math. Lanes of a partial last tile redo the last row (so
+// shuffles stay converged) but store nothing.
+//
+// Launch: the kernels are launched with programmatic stream serialization.
+// A block fills its shared tables, lets dependent launches begin
+// (griddepcontrol.launch_dependents), then waits for the grids it depends on
+// to complete (griddepcontrol.wait) before touching any input or output, so
+// the prologue overlaps the previous kernel's tail and stream order holds.
 #pragma once
 
 #include "tq_device.cuh"
@@ -33,21 +43,34 @@
 namespace tq {
 
 constexpr int kThreads = 256;
+#ifndef TQ_ENCODE_MIN_BLOCKS
+#define TQ_ENCODE_MIN_BLOCKS 3  // 24 resident warps per SM
+#endif
+#ifndef TQ_DECODE_MIN_BLOCKS
+#define TQ_DECODE_MIN_BLOCKS 3  // 24 resident warps per SM
+#endif
+constexpr int kEncodeMinBlocks = TQ_ENCODE_MIN_BLOCKS;
+constexpr int kDecodeMinBlocks = TQ_DECODE_MIN_BLOCKS;
 
-template <int KB, bool SIGNED>
-struct KeyLevels {
-  static constexpr int kMax = SIGNED ? (1 << (KB - 1)) - 1 : (1 << KB) - 1;
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <int KMODE>
+struct KeySpec {
+  static constexpr int B = (KMODE == kK2) ? 2 : (KMODE == kK4) ? 4 : (KMODE == kK5) ? 5 : 8;
+  static constexpr bool SIGNED = (KMODE == kK8Signed);
+  static constexpr int kMax = SIGNED ? (1 << (B - 1)) - 1 : (1 << B) - 1;
   static constexpr int kLo = SIGNED ? -kMax : 0;
   static constexpr int kHi = kMax;
 };
 
 // Exact per-element quantisation (the page's operations, IEEE division).
-template <int KB, bool SIGNED>
+template <int KMODE>
 __device__ __forceinline__ uint32_t key_code_exact(float x, float se, float zp) {
-  using L = KeyLevels<KB, SIGNED>;
+  using M = KeySpec<KMODE>;
   float r = rintf(__fsub_rn(__fdiv_rn(x, se), zp));
-  r = (r < static_cast<float>(L::kLo)) ? static_cast<float>(L::kLo) : r;
-  r = (r > static_cast<float>(L::kHi)) ? static_cast<float>(L::kHi) : r;
+  r = (r < static_cast<float>(M::kLo)) ? static_cast<float>(M::kLo) : r;
+  r = (r > static_cast<float>(M::kHi)) ? static_cast<float>(M::kHi) : r;
   return static_cast<uint32_t>(static_cast<int>(r));
 }
 
@@ -65,20 +88,78 @@ __device__ __forceinline__ void scan_min_max(const float2 (&X)[16], float& mn, f
   }
 }
 
-// K encode of one group held by this lane; X = pairs (element p, p + 16).
-template <int KB, bool SIGNED>
-__device__ __forceinline__ void encode_key_group(const float2 (&X)[16], float mn, float mx, bool store,
-                                                 uint8_t* codes, uint16_t* scale_out, uint16_t* zero_out) {
-  using L = KeyLevels<KB, SIGNED>;
+// One item's inputs: 16 words of bf16 pairs, or 32 fp32 values.
+template <bool F32>
+struct ItemIn {
+  uint32_t w[F32 ? 32 : 16];
+};
+
+template <bool F32>
+__device__ __forceinline__ void load_item(const void* base, size_t elem_off, ItemIn<F32>& in) {
+  if constexpr (F32) {
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + elem_off);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 u = __ldg(q + i);
+      in.w[4 * i] = u.x; in.w[4 * i + 1] = u.y; in.w[4 * i + 2] = u.z; in.w[4 * i + 3] = u.w;
+    }
+  } else {
+    load_words16(static_cast<const __nv_bfloat16*>(base) + elem_off, in.w);
+  }
+}
+
+template <bool F32>
+__device__ __forceinline__ void item_to_pairs(const ItemIn<F32>& in, float2 (&P)[16]) {
+  if constexpr (F32) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) P[q] = make_float2(__uint_as_float(in.w[q]), __uint_as_float(in.w[q + 16]));
+  } else {
+    words_to_pairs(in.w, P);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K encode of the group held by this lane. `prefetch` runs once the inputs
+// are in registers (it may overwrite `in`).
+template <int KMODE, bool F32, typename Prefetch>
+__device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, bool store, uint8_t* codes, uint16_t* scale_out,
+                                                uint16_t* zero_out, Prefetch&& prefetch) {
+  using M = KeySpec<KMODE>;
+  float2 X[16];
+  float mn, mx;
+  if constexpr (F32) {
+    mn = __uint_as_float(in.w[0]);
+    mx = mn;
+#pragma unroll
+    for (int i = 1; i < 32; ++i) {
+      mn = fminf(mn, __uint_as_float(in.w[i]));
+      mx = fmaxf(mx, __uint_as_float(in.w[i]));
+    }
+  } else {
+    // min / max on bf16 pairs (exact: the upcast preserves order)
+    __nv_bfloat162 lo2 = *reinterpret_cast<const __nv_bfloat162*>(&in.w[0]);
+    __nv_bfloat162 hi2 = lo2;
+#pragma unroll
+    for (int j = 1; j < 16; ++j) {
+      const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&in.w[j]);
+      lo2 = __hmin2(lo2, v2);
+      hi2 = __hmax2(hi2, v2);
+    }
+    mn = fminf(__low2float(lo2), __high2float(lo2));
+    mx = fmaxf(__low2float(hi2), __high2float(hi2));
+  }
+  item_to_pairs(in, X);
+  prefetch();
   if (mn == 0.0f || mx == 0.0f) scan_min_max(X, mn, mx);
+
   const float range = __fsub_rn(mx, mn);
   float scale, zp;
-  if constexpr (SIGNED) {
-    scale = __fdiv_rn(range, static_cast<float>(2 * L::kMax));
+  if constexpr (M::SIGNED) {
+    scale = __fdiv_rn(range, static_cast<float>(2 * M::kMax));
     const float denom = __fmul_rn(2.0f, __fadd_rn(scale, kEps));
     zp = rintf(__fdiv_rn(__fadd_rn(mx, mn), denom));
   } else {
-    scale = __fdiv_rn(range, static_cast<float>(L::kMax));
+    scale = __fdiv_rn(range, static_cast<float>(M::kMax));
     zp = rintf(__fdiv_rn(mn, __fadd_rn(scale, kEps)));
   }
   const float se = __fadd_rn(scale, kEps);
@@ -87,40 +168,99 @@ __device__ __forceinline__ void encode_key_group(const float2 (&X)[16], float mn
   const float amax = fmaxf(fabsf(mn), fabsf(mx));
   const float band = __fmul_rn(__fadd_rn(__fmul_rn(amax, inv), fabsf(zp)), 2.5e-7f);
   const float thr = __fsub_rn(0.5f, band);
-  const int lo_bits = static_cast<int>(kMagicBits) + L::kLo;
-  const int hi_bits = static_cast<int>(kMagicBits) + L::kHi;
+  const int lo_bits = static_cast<int>(kMagicBits) + M::kLo;
+  const int hi_bits = static_cast<int>(kMagicBits) + M::kHi;
+  // t = RN(x * inv - zp) is monotone in x, so when the group's min and max
+  // round inside the code range every element does and no clamp is needed.
+  const float2 ext = add2(fma2(make_float2(mn, mx), f2(inv), f2(-zp)), f2(kMagic));
+  const bool in_range = __float_as_int(ext.x) >= lo_bits && __float_as_int(ext.y) <= hi_bits;
 
-  uint32_t w[KB];
+  uint32_t w[M::B];
 #pragma unroll
-  for (int k = 0; k < KB; ++k) w[k] = 0;
+  for (int k = 0; k < M::B; ++k) w[k] = 0;
   bool ok = true;
+  if (__all_sync(kFull, in_range)) {
 #pragma unroll
-  for (int p = 0; p < 16; ++p) {
-    const float2 t = fma2(X[p], f2(inv), f2(-zp));
-    const float2 s = add2(t, f2(kMagic));
-    const float2 d = sub2(t, sub2(s, f2(kMagic)));
-    ok = ok && (fabsf(d.x) < thr) && (fabsf(d.y) < thr);
-    put_code<KB>(w, p, static_cast<uint32_t>(min(max(__float_as_int(s.x), lo_bits), hi_bits)));
-    put_code<KB>(w, p + 16, static_cast<uint32_t>(min(max(__float_as_int(s.y), lo_bits), hi_bits)));
+    for (int q = 0; q < 16; ++q) {
+      const float2 t = fma2(X[q], f2(inv), f2(-zp));
+      const float2 s = add2(t, f2(kMagic));
+      const float2 d = sub2(t, sub2(s, f2(kMagic)));
+      ok = ok && (fabsf(d.x) < thr) && (fabsf(d.y) < thr);
+      put_code<M::B>(w, q, static_cast<uint32_t>(__float_as_int(s.x)));
+      put_code<M::B>(w, q + 16, static_cast<uint32_t>(__float_as_int(s.y)));
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float2 t = fma2(X[q], f2(inv), f2(-zp));
+      const float2 s = add2(t, f2(kMagic));
+      const float2 d = sub2(t, sub2(s, f2(kMagic)));
+      ok = ok && (fabsf(d.x) < thr) && (fabsf(d.y) < thr);
+      put_code<M::B>(w, q, static_cast<uint32_t>(min(max(__float_as_int(s.x), lo_bits), hi_bits)));
+      put_code<M::B>(w, q + 16, static_cast<uint32_t>(min(max(__float_as_int(s.y), lo_bits), hi_bits)));
+    }
   }
-  if (!ok) {
+  if (!ok) {  // rare: an element within the guard band of a rounding tie
 #pragma unroll
-    for (int k = 0; k < KB; ++k) w[k] = 0;
+    for (int k = 0; k < M::B; ++k) w[k] = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) put_code<KB>(w, i, key_code_exact<KB, SIGNED>(pair_elem(X, i), se, zp));
+    for (int i = 0; i < 32; ++i) put_code<M::B>(w, i, key_code_exact<KMODE>(pair_elem(X, i), se, zp));
   }
   if (store) {
-    store_words<KB>(codes, w);
+    store_words<M::B>(codes, w);
     *scale_out = __half_as_ushort(__float2half_rn(scale));
     *zero_out = __half_as_ushort(__float2half_rn(zp));
   }
 }
 
-// ---------------------------------------------------------------------------
-template <int D, int VB, bool BF16>
-__global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
+// V encode of the group held by this lane (the whole row's lanes rotate together).
+template <int LPR, int VB, bool F32, typename Prefetch>
+__device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const uint32_t* s_sign,
+                                                  const CellEntry* s_cells, float rot_scale, float neg_zero,
+                                                  bool store, uint8_t* codes, uint16_t* scale_out,
+                                                  Prefetch&& prefetch) {
+  uint32_t S[16];
+  load_sign_words(s_sign, l, S);
+  float2 Y[16];
+  if constexpr (F32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) in.w[i] ^= elem_sign(S, i);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) in.w[j] ^= S[j];
+  }
+  item_to_pairs(in, Y);
+  prefetch();
+  hadamard_row<LPR>(Y, l);
+  const float2 c2 = f2(rot_scale);
+#pragma unroll
+  for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
+  const float rms = __fsqrt_rn(__fmul_rn(group_sum_sq(Y, f2(neg_zero)), 1.0f / kGroup));  // /32 is exact
+  const float inv = __frcp_rn(__fadd_rn(rms, kEps));
+  uint32_t w[VB];
+#pragma unroll
+  for (int k = 0; k < VB; ++k) w[k] = 0;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    int i0, i1;
+    lm_index2_scaled<VB>(Y[q], inv, s_cells, i0, i1);
+    put_code<VB>(w, q, static_cast<uint32_t>(i0));
+    put_code<VB>(w, q + 16, static_cast<uint32_t>(i1));
+  }
+  if (store) {
+    store_words<VB>(codes, w);
+    *scale_out = __half_as_ushort(__float2half_rn(rms));
+  }
+}
+
+template <int D, int VB, int KMODE, bool F32>
+__global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(EncodeParams p) {
   using G = Geo<D>;
+  using M = KeySpec<KMODE>;
   constexpr int NC = CellGrid<VB>::NC;
+  constexpr int pdk = D * M::B / 8;
+  constexpr int pdv = D * VB / 8;
+  constexpr int NG = D / kGroup;
   __shared__ CellEntry s_cells[NC];
   __shared__ __align__(16) uint32_t s_sign[D / 2];
   {
@@ -129,144 +269,119 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
     fill_sign_words<D>(s_sign);
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int lane = threadIdx.x & 31;
   const int sub = lane / G::LPR;
   const int l = lane % G::LPR;
-
-  const int pdk = D * ((p.kmode == kK2) ? 2 : (p.kmode == kK4) ? 4 : (p.kmode == kK5) ? 5 : 8) / 8;
-  const int kbytes = pdk / G::LPR;  // packed key bytes of one group
-  constexpr int pdv = D * VB / 8;
-  constexpr int NG = D / kGroup;
-  const int warps_per_block = blockDim.x >> 5;
-  const int n_warps = gridDim.x * warps_per_block;
+  const int n_warps = gridDim.x * (blockDim.x >> 5);
   const int tiles = (p.rows + G::RPW - 1) / G::RPW;
+  const int items = 2 * tiles;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
-  for (int tile = blockIdx.x * warps_per_block + (threadIdx.x >> 5); tile < tiles; tile += n_warps) {
-    const int r0 = tile * G::RPW + sub;
+  // item -> row of this lane (clamped to the last row for a partial tile)
+  auto item_row = [&](int it) { const int r0 = (it >> 1) * G::RPW + sub; return r0 < p.rows ? r0 : p.rows - 1; };
+  ItemIn<F32> in;
+  int step = 0;
+  if (gw < items) {
+    const bool v0 = ((gw ^ step) & 1) != 0;
+    load_item<F32>(v0 ? p.v : p.k, static_cast<size_t>(item_row(gw)) * D + kGroup * l, in);
+  }
+  for (int it = gw; it < items; it += n_warps, ++step) {
+    const bool is_v = ((it ^ step) & 1) != 0;
+    const int r0 = (it >> 1) * G::RPW + sub;
     const bool valid = r0 < p.rows;
     const int r = valid ? r0 : p.rows - 1;
     const int bh = fast_div(r, p.tdiv);
-    const int t = r - bh * p.T;
-    const long long orow = static_cast<long long>(bh) * p.t_cap + p.t_off + t;
-    const size_t in_off = static_cast<size_t>(r) * D + kGroup * l;
+    const long long orow = static_cast<long long>(bh) * p.t_cap + p.t_off + (r - bh * p.T);
 
-    // loads of both K and V are issued up front
-    uint32_t wk[16], wv[16];
-    float xk[BF16 ? 1 : 32], xv[BF16 ? 1 : 32];
-    if constexpr (BF16) {
-      load_words16(static_cast<const __nv_bfloat16*>(p.k) + in_off, wk);
-      load_words16(static_cast<const __nv_bfloat16*>(p.v) + in_off, wv);
+    const int nx = it + n_warps;
+    // the next item's loads are issued once this item's inputs are converted,
+    // so they overlap this item's math
+    auto prefetch = [&]() {
+      if (nx < items) {
+        const bool nv = ((nx ^ (step + 1)) & 1) != 0;
+        load_item<F32>(nv ? p.v : p.k, static_cast<size_t>(item_row(nx)) * D + kGroup * l, in);
+      }
+    };
+    if (!is_v) {
+      encode_key_item<KMODE, F32>(in, valid, p.k_codes + orow * pdk + 4 * M::B * l, p.k_scales + orow * NG + l,
+                                  p.k_zeros + orow * NG + l, prefetch);
     } else {
-      load_floats32(static_cast<const float*>(p.k) + in_off, xk);
-      load_floats32(static_cast<const float*>(p.v) + in_off, xv);
-    }
-
-    // ---- keys
-    {
-      float2 X[16];
-      float mn, mx;
-      if constexpr (BF16) {
-        // min / max on bf16 pairs (exact: the upcast preserves order)
-        __nv_bfloat162 lo2 = *reinterpret_cast<const __nv_bfloat162*>(&wk[0]);
-        __nv_bfloat162 hi2 = lo2;
-#pragma unroll
-        for (int j = 1; j < 16; ++j) {
-          const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&wk[j]);
-          lo2 = __hmin2(lo2, v2);
-          hi2 = __hmax2(hi2, v2);
-        }
-        mn = fminf(__low2float(lo2), __high2float(lo2));
-        mx = fmaxf(__low2float(hi2), __high2float(hi2));
-        words_to_pairs(wk, X);
-      } else {
-        mn = xk[0];
-        mx = xk[0];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) {
-          mn = fminf(mn, xk[i]);
-          mx = fmaxf(mx, xk[i]);
-        }
-        floats_to_pairs(xk, X);
-      }
-      uint8_t* codes = p.k_codes + orow * pdk + kbytes * l;
-      uint16_t* sc = p.k_scales + orow * NG + l;
-      uint16_t* zr = p.k_zeros + orow * NG + l;
-      switch (p.kmode) {
-        case kK2: encode_key_group<2, false>(X, mn, mx, valid, codes, sc, zr); break;
-        case kK4: encode_key_group<4, false>(X, mn, mx, valid, codes, sc, zr); break;
-        case kK5: encode_key_group<5, false>(X, mn, mx, valid, codes, sc, zr); break;
-        case kK8: encode_key_group<8, false>(X, mn, mx, valid, codes, sc, zr); break;
-        default: encode_key_group<8, true>(X, mn, mx, valid, codes, sc, zr); break;
-      }
-    }
-
-    // ---- values
-    {
-      uint32_t S[16];
-      load_sign_words(s_sign, l, S);
-      float2 Y[16];
-      if constexpr (BF16) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) wv[j] ^= S[j];
-        words_to_pairs(wv, Y);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] = __uint_as_float(__float_as_uint(xv[i]) ^ elem_sign(S, i));
-        floats_to_pairs(xv, Y);
-      }
-      hadamard_row<G::LPR>(Y, l);
-      const float2 c2 = f2(p.rot_scale);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
-      const float2 nz = f2(p.neg_zero);
-      const float rms = __fsqrt_rn(__fmul_rn(group_sum_sq(Y, nz), 1.0f / kGroup));  // /32 is exact
-      const float inv = __frcp_rn(__fadd_rn(rms, kEps));
-      uint32_t w[VB];
-#pragma unroll
-      for (int k2 = 0; k2 < VB; ++k2) w[k2] = 0;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        int i0, i1;
-        lm_index2<VB>(mul0(Y[q], f2(inv), nz), s_cells, i0, i1);
-        put_code<VB>(w, q, static_cast<uint32_t>(i0));
-        put_code<VB>(w, q + 16, static_cast<uint32_t>(i1));
-      }
-      if (valid) {
-        store_words<VB>(p.v_codes + orow * pdv + 4 * VB * l, w);
-        p.v_scales[orow * NG + l] = __half_as_ushort(__float2half_rn(rms));
-      }
+      encode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cells, p.rot_scale, p.neg_zero, valid,
+                                         p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l, prefetch);
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
-// Codes become floats through the 1.5 * 2^23 encoding (exact for |q| < 2^22).
-template <int KB, bool SIGNED>
-__device__ __forceinline__ void decode_key_group(const uint8_t* codes, float z, float s, float (&x)[32]) {
-  uint32_t w[KB];
-  load_words<KB>(codes, w);
+// Decode. An item's inputs: the packed words of the group and its fp16 scale
+// (and zero point for K).
+template <int WORDS>
+struct PackedIn {
+  uint32_t w[WORDS];
+  uint32_t sz;  // scale in the low half, zero point (K) in the high half
+};
+
+template <int KB, int VB>
+__device__ __forceinline__ void load_packed_item(const DecodeParams& p, bool is_v, long long irow, int l,
+                                                 PackedIn<(KB > VB ? KB : VB)>& in) {
+  constexpr int W = KB > VB ? KB : VB;
+  if (is_v) {
+    uint32_t t[VB];
+    load_words<VB>(p.v_codes + irow * p.pdv + 4 * VB * l, t);
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    int q0 = static_cast<int>(unpack_code<KB>(w, i));
-    int q1 = static_cast<int>(unpack_code<KB>(w, i + 1));
-    if constexpr (SIGNED) {
-      q0 = static_cast<int>(static_cast<int8_t>(q0));
-      q1 = static_cast<int>(static_cast<int8_t>(q1));
-    }
-    float2 f = make_float2(__int_as_float(static_cast<int>(kMagicBits) + q0),
-                           __int_as_float(static_cast<int>(kMagicBits) + q1));
-    f = sub2(f, f2(kMagic));                 // the code, exactly
-    f = mul2(add2(f, f2(z)), f2(s));         // (code + zero) * scale
-    x[i] = f.x;
-    x[i + 1] = f.y;
+    for (int k = 0; k < W; ++k) in.w[k] = (k < VB) ? t[k < VB ? k : 0] : 0u;
+    in.sz = __ldg(p.v_scales + irow * p.ng + l);
+  } else {
+    uint32_t t[KB];
+    load_words<KB>(p.k_codes + irow * p.pdk + 4 * KB * l, t);
+#pragma unroll
+    for (int k = 0; k < W; ++k) in.w[k] = (k < KB) ? t[k < KB ? k : 0] : 0u;
+    in.sz = static_cast<uint32_t>(__ldg(p.k_scales + irow * p.ng + l)) |
+            (static_cast<uint32_t>(__ldg(p.k_zeros + irow * p.ng + l)) << 16);
   }
 }
 
-template <bool BF16>
+// K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
+// Codes become floats through the 1.5 * 2^23 encoding (exact for |q| < 2^22).
+// `prefetch` runs once the packed inputs are consumed (it may overwrite `in`).
+template <int KMODE, int W, typename Prefetch>
+__device__ __forceinline__ void decode_key_item(const PackedIn<W>& in, float (&x)[32], Prefetch&& prefetch) {
+  using M = KeySpec<KMODE>;
+  const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz & 0xffffu)));
+  const float z = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz >> 16)));
+  float2 f[16];
+  {
+    uint32_t w[M::B];
+#pragma unroll
+    for (int k = 0; k < M::B; ++k) w[k] = in.w[k];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      int q0 = static_cast<int>(unpack_code<M::B>(w, i));
+      int q1 = static_cast<int>(unpack_code<M::B>(w, i + 1));
+      if constexpr (M::SIGNED) {
+        q0 = static_cast<int>(static_cast<int8_t>(q0));
+        q1 = static_cast<int>(static_cast<int8_t>(q1));
+      }
+      f[i / 2] = make_float2(__int_as_float(static_cast<int>(kMagicBits) + q0),
+                             __int_as_float(static_cast<int>(kMagicBits) + q1));
+    }
+  }
+  prefetch();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float2 g = sub2(f[i], f2(kMagic));   // the code, exactly
+    g = mul2(add2(g, f2(z)), f2(s));     // (code + zero) * scale
+    x[2 * i] = g.x;
+    x[2 * i + 1] = g.y;
+  }
+}
+
+template <bool F32>
 __device__ __forceinline__ void store_group(void* base, size_t off, const float (&x)[32]) {
-  if constexpr (BF16) {
+  if constexpr (!F32) {
     uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -283,92 +398,101 @@ __device__ __forceinline__ void store_group(void* base, size_t off, const float 
   }
 }
 
-template <int D, int VB, bool BF16>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
+template <int LPR, int VB, bool F32, int W, typename Prefetch>
+__device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, const uint32_t* s_sign,
+                                                  const float* s_cent, float rot_scale, float neg_zero,
+                                                  bool store, void* out, size_t out_off, Prefetch&& prefetch) {
+  const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz & 0xffffu)));
+  const float2 nz = f2(neg_zero);
+  float2 Y[16];
+  {
+    uint32_t w[VB];
+#pragma unroll
+    for (int k = 0; k < VB; ++k) w[k] = in.w[k];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) Y[q] = make_float2(s_cent[unpack_code<VB>(w, q)], s_cent[unpack_code<VB>(w, q + 16)]);
+  }
+  prefetch();
+#pragma unroll
+  for (int q = 0; q < 16; ++q) Y[q] = mul0(Y[q], f2(s), nz);  // feeds the butterflies: must stay rounded
+  hadamard_row<LPR>(Y, l);
+  const float2 c2 = f2(rot_scale);
+#pragma unroll
+  for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
+  uint32_t S[16];
+  load_sign_words(s_sign, l, S);
+  if (!store) return;
+  if constexpr (!F32) {
+    // round to bf16, then apply the signs on the packed words (exact)
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(Y[2 * j].x, Y[2 * j + 1].x);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(Y[2 * j].y, Y[2 * j + 1].y);
+      o[j] = *reinterpret_cast<const uint32_t*>(&a) ^ S[j];
+      o[j + 8] = *reinterpret_cast<const uint32_t*>(&b) ^ S[j + 8];
+    }
+    uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + out_off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  } else {
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(S, i));
+    store_group<true>(out, out_off, x);
+  }
+}
+
+template <int D, int VB, int KMODE, bool F32>
+__global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(DecodeParams p) {
   using G = Geo<D>;
+  using M = KeySpec<KMODE>;
   constexpr int NCENT = 1 << VB;
+  constexpr int W = M::B > VB ? M::B : VB;
   __shared__ float s_cent[NCENT];
   __shared__ __align__(16) uint32_t s_sign[D / 2];
   for (int i = threadIdx.x; i < NCENT; i += blockDim.x) s_cent[i] = centroid_table<VB>()[i];
   fill_sign_words<D>(s_sign);
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int lane = threadIdx.x & 31;
   const int sub = lane / G::LPR;
   const int l = lane % G::LPR;
-
-  const int pdk = D * ((p.kmode == kK2) ? 2 : (p.kmode == kK4) ? 4 : (p.kmode == kK5) ? 5 : 8) / 8;
-  const int kbytes = pdk / G::LPR;
-  constexpr int pdv = D * VB / 8;
-  constexpr int NG = D / kGroup;
-  const int warps_per_block = blockDim.x >> 5;
-  const int n_warps = gridDim.x * warps_per_block;
+  const int n_warps = gridDim.x * (blockDim.x >> 5);
   const int tiles = (p.rows + G::RPW - 1) / G::RPW;
+  const int items = 2 * tiles;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
-  for (int tile = blockIdx.x * warps_per_block + (threadIdx.x >> 5); tile < tiles; tile += n_warps) {
-    const int r0 = tile * G::RPW + sub;
+  auto item_irow = [&](int it) {
+    const int r0 = (it >> 1) * G::RPW + sub;
+    const int r = r0 < p.rows ? r0 : p.rows - 1;
+    const int bh = fast_div(r, p.tdiv);
+    return static_cast<long long>(bh) * p.t_cap + (r - bh * p.T);
+  };
+  PackedIn<W> in;
+  int step = 0;
+  if (gw < items) load_packed_item<M::B, VB>(p, ((gw ^ step) & 1) != 0, item_irow(gw), l, in);
+  for (int it = gw; it < items; it += n_warps, ++step) {
+    const bool is_v = ((it ^ step) & 1) != 0;
+    const int r0 = (it >> 1) * G::RPW + sub;
     const bool valid = r0 < p.rows;
     const int r = valid ? r0 : p.rows - 1;
-    const int bh = fast_div(r, p.tdiv);
-    const int t = r - bh * p.T;
-    const long long irow = static_cast<long long>(bh) * p.t_cap + t;
     const size_t out_off = static_cast<size_t>(r) * D + kGroup * l;
 
-    // ---- keys
-    {
-      const uint8_t* codes = p.k_codes + irow * pdk + kbytes * l;
-      const float z = __half2float(__ushort_as_half(__ldg(p.k_zeros + irow * NG + l)));
-      const float s = __half2float(__ushort_as_half(__ldg(p.k_scales + irow * NG + l)));
+    const int nx = it + n_warps;
+    // the next item's loads are issued once this item's inputs are consumed
+    auto prefetch = [&]() {
+      if (nx < items) load_packed_item<M::B, VB>(p, ((nx ^ (step + 1)) & 1) != 0, item_irow(nx), l, in);
+    };
+    if (!is_v) {
       float x[32];
-      switch (p.kmode) {
-        case kK2: decode_key_group<2, false>(codes, z, s, x); break;
-        case kK4: decode_key_group<4, false>(codes, z, s, x); break;
-        case kK5: decode_key_group<5, false>(codes, z, s, x); break;
-        case kK8: decode_key_group<8, false>(codes, z, s, x); break;
-        default: decode_key_group<8, true>(codes, z, s, x); break;
-      }
-      if (valid) store_group<BF16>(p.k_out, out_off, x);
-    }
-
-    // ---- values
-    {
-      uint32_t w[VB];
-      load_words<VB>(p.v_codes + irow * pdv + 4 * VB * l, w);
-      const float s = __half2float(__ushort_as_half(__ldg(p.v_scales + irow * NG + l)));
-      float2 Y[16];
-      const float2 nz = f2(p.neg_zero);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float2 c = make_float2(s_cent[unpack_code<VB>(w, q)], s_cent[unpack_code<VB>(w, q + 16)]);
-        Y[q] = mul0(c, f2(s), nz);  // feeds the butterflies: must stay rounded
-      }
-      hadamard_row<G::LPR>(Y, l);
-      const float2 c2 = f2(p.rot_scale);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
-      uint32_t S[16];
-      load_sign_words(s_sign, l, S);
-      if (valid) {
-        if constexpr (BF16) {
-          // round to bf16, then apply the signs on the packed words (exact)
-          uint32_t o[16];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const __nv_bfloat162 a = __floats2bfloat162_rn(Y[2 * j].x, Y[2 * j + 1].x);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(Y[2 * j].y, Y[2 * j + 1].y);
-            o[j] = *reinterpret_cast<const uint32_t*>(&a) ^ S[j];
-            o[j + 8] = *reinterpret_cast<const uint32_t*>(&b) ^ S[j + 8];
-          }
-          uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_out) + out_off);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        } else {
-          float x[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(S, i));
-          store_group<false>(p.v_out, out_off, x);
-        }
-      }
+      decode_key_item<KMODE>(in, x, prefetch);
+      if (valid) store_group<F32>(p.k_out, out_off, x);
+    } else {
+      decode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cent, p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
+                                         prefetch);
     }
   }
 }
@@ -382,65 +506,95 @@ inline int resident_blocks(K kernel) {
   return per_sm * sm_count();
 }
 
-inline int grid_for(long long tiles, int resident) {
-  const long long needed = (tiles + (kThreads / 32) - 1) / (kThreads / 32);
+inline int grid_for(long long items, int resident) {
+  const long long needed = (items + (kThreads / 32) - 1) / (kThreads / 32);
   return static_cast<int>(needed < resident ? needed : resident);
 }
 
-template <int D, int VB, bool BF16>
-cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
-  static const int resident = resident_blocks(encode_kernel<D, VB, BF16>);
-  const long long tiles = (p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW;
-  encode_kernel<D, VB, BF16><<<grid_for(tiles, resident), kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+// Launch with programmatic stream serialization (see the file comment).
+template <typename Params>
+inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D, int VB, bool BF16>
+template <int D, int VB, int KMODE, bool F32>
+cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
+  static const int resident = resident_blocks(encode_kernel<D, VB, KMODE, F32>);
+  const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
+  const cudaError_t e = launch_pdl(encode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D, int VB, int KMODE, bool F32>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
-  static const int resident = resident_blocks(decode_kernel<D, VB, BF16>);
-  const long long tiles = (p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW;
-  decode_kernel<D, VB, BF16><<<grid_for(tiles, resident), kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  static const int resident = resident_blocks(decode_kernel<D, VB, KMODE, F32>);
+  const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
+  const cudaError_t e = launch_pdl(decode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D, int VB, bool F32>
+cudaError_t launch_encode_vb(const EncodeParams& p, cudaStream_t s) {
+  switch (p.kmode) {
+    case kK2: return launch_encode_t<D, VB, kK2, F32>(p, s);
+    case kK4: return launch_encode_t<D, VB, kK4, F32>(p, s);
+    case kK5: return launch_encode_t<D, VB, kK5, F32>(p, s);
+    case kK8: return launch_encode_t<D, VB, kK8, F32>(p, s);
+    default: return launch_encode_t<D, VB, kK8Signed, F32>(p, s);
+  }
+}
+
+template <int D, int VB, bool F32>
+cudaError_t launch_decode_vb(const DecodeParams& p, cudaStream_t s) {
+  switch (p.kmode) {
+    case kK2: return launch_decode_t<D, VB, kK2, F32>(p, s);
+    case kK4: return launch_decode_t<D, VB, kK4, F32>(p, s);
+    case kK5: return launch_decode_t<D, VB, kK5, F32>(p, s);
+    case kK8: return launch_decode_t<D, VB, kK8, F32>(p, s);
+    default: return launch_decode_t<D, VB, kK8Signed, F32>(p, s);
+  }
+}
+
+template <int D, bool F32>
+cudaError_t launch_encode_dt(const EncodeParams& p, int v_bits, cudaStream_t s) {
+  switch (v_bits) {
+    case 2: return launch_encode_vb<D, 2, F32>(p, s);
+    case 3: return launch_encode_vb<D, 3, F32>(p, s);
+    case 4: return launch_encode_vb<D, 4, F32>(p, s);
+    case 5: return launch_encode_vb<D, 5, F32>(p, s);
+    default: return launch_encode_vb<D, 8, F32>(p, s);
+  }
+}
+
+template <int D, bool F32>
+cudaError_t launch_decode_dt(const DecodeParams& p, int v_bits, cudaStream_t s) {
+  switch (v_bits) {
+    case 2: return launch_decode_vb<D, 2, F32>(p, s);
+    case 3: return launch_decode_vb<D, 3, F32>(p, s);
+    case 4: return launch_decode_vb<D, 4, F32>(p, s);
+    case 5: return launch_decode_vb<D, 5, F32>(p, s);
+    default: return launch_decode_vb<D, 8, F32>(p, s);
+  }
 }
 
 template <int D>
 cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaStream_t s) {
-  if (in_bf16) {
-    switch (v_bits) {
-      case 2: return launch_encode_t<D, 2, true>(p, s);
-      case 3: return launch_encode_t<D, 3, true>(p, s);
-      case 4: return launch_encode_t<D, 4, true>(p, s);
-      case 5: return launch_encode_t<D, 5, true>(p, s);
-      default: return launch_encode_t<D, 8, true>(p, s);
-    }
-  }
-  switch (v_bits) {
-    case 2: return launch_encode_t<D, 2, false>(p, s);
-    case 3: return launch_encode_t<D, 3, false>(p, s);
-    case 4: return launch_encode_t<D, 4, false>(p, s);
-    case 5: return launch_encode_t<D, 5, false>(p, s);
-    default: return launch_encode_t<D, 8, false>(p, s);
-  }
+  return in_bf16 ? launch_encode_dt<D, false>(p, v_bits, s) : launch_encode_dt<D, true>(p, v_bits, s);
 }
 
 template <int D>
 cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, cudaStream_t s) {
-  if (out_bf16) {
-    switch (v_bits) {
-      case 2: return launch_decode_t<D, 2, true>(p, s);
-      case 3: return launch_decode_t<D, 3, true>(p, s);
-      case 4: return launch_decode_t<D, 4, true>(p, s);
-      case 5: return launch_decode_t<D, 5, true>(p, s);
-      default: return launch_decode_t<D, 8, true>(p, s);
-    }
-  }
-  switch (v_bits) {
-    case 2: return launch_decode_t<D, 2, false>(p, s);
-    case 3: return launch_decode_t<D, 3, false>(p, s);
-    case 4: return launch_decode_t<D, 4, false>(p, s);
-    case 5: return launch_decode_t<D, 5, false>(p, s);
-    default: return launch_decode_t<D, 8, false>(p, s);
-  }
+  return out_bf16 ? launch_decode_dt<D, false>(p, v_bits, s) : launch_decode_dt<D, true>(p, v_bits, s);
 }
 
 }  // namespace tq
