@@ -320,6 +320,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e["ms"], dev)
     e2e_value = tokens_per_step * e2e["steps"] * ws / (e2e_ms / 1e3)
 
+    workloads = run_other_workloads(tq, dev, stream, peak) if args.workloads else None
+
     cpu = None
     if rank == 0 and ws == 1:
         rows_done, secs = oracle_timing(rows, args.cpu_seconds, 3 * args.cpu_seconds)
@@ -347,6 +349,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"]},
             "cpu_baseline": cpu,
+            "workloads": workloads,
             "gpu_launches": 2 * LAYERS * args.steps,
             "clocks": clocks,
         }
@@ -354,6 +357,70 @@ def run_ours(args):
     barrier()
     if torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()
+
+
+def _time_launches(fn, stream, reps):
+    """Average ms of fn() (one launch) over reps back-to-back launches, events on `stream`."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        fn()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_other_workloads(tq, dev, stream, peak):
+    """The other benchmark workloads, one launch at a time (inputs far larger
+    than L2): encode and decode GB/s (algorithmic bytes) and fraction of the
+    HBM peak, plus the long-context decode-step append latency."""
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_append_steps, make_kv
+
+    out = {}
+    for name in ("long_context", "hd256", "hd512"):
+        w = WORKLOADS[name]
+        k, v = make_kv(w, device=dev)
+        ko, vo = torch.empty_like(k), torch.empty_like(v)
+        rows = w.rows
+        for vb in w.v_bits:
+            t_cap = w.t_cap or w.T
+            cache = tq.alloc_cache(w.B, w.H, t_cap, w.D, w.k_bits, vb, device=dev)
+            bpl = rows * bytes_per_row(w.D, w.k_bits, vb, 2)
+            enc = _time_launches(lambda: tq.tq_encode_kv(k, v, w.k_bits, w.k_signed, vb, cache, stream=stream),
+                                 stream, 10)
+            dec = _time_launches(lambda: tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo,
+                                                         stream=stream), stream, 10)
+            r = {"shape": [w.B, w.H, w.T, w.D], "k_bits": w.k_bits, "v_bits": vb, "bytes_per_launch": bpl,
+                 "encode_us": 1e3 * enc, "decode_us": 1e3 * dec,
+                 "encode_GBps": bpl / (enc * 1e-3) / 1e9, "decode_GBps": bpl / (dec * 1e-3) / 1e9,
+                 "encode_tokens_per_s": w.tokens / (enc * 1e-3), "decode_tokens_per_s": w.tokens / (dec * 1e-3)}
+            r["encode_frac"] = r["encode_GBps"] / peak
+            r["decode_frac"] = r["decode_GBps"] / peak
+            if name == "long_context":
+                # decode-step appends: one token per sequence at t_off = T + s
+                steps = [(a.to(dev), b.to(dev)) for a, b in make_append_steps(w)]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    for s_, (a, b) in enumerate(steps):
+                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
+                torch.cuda.synchronize(dev)
+                with torch.cuda.graph(g, stream=stream):
+                    for s_, (a, b) in enumerate(steps):
+                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
+                ms = _time_launches(g.replay, stream, 20)
+                r["append_us_per_step"] = 1e3 * ms / len(steps)
+                r["append_rows_per_step"] = w.B * w.H
+                # the full cache after the appends decodes like the rest
+                dec_all = _time_launches(lambda: tq.tq_decode_kv(cache, t_cap, w.k_bits, w.k_signed, vb,
+                                                                 stream=stream), stream, 3)
+                r["decode_full_cache_us"] = 1e3 * dec_all
+            out["%s_v%d" % (name, vb)] = r
+            del cache
+        del k, v, ko, vo
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
@@ -397,6 +464,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the secondary long-context / hd256 / hd512 measurements")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
