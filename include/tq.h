@@ -86,6 +86,29 @@ tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_
                        int k_bits, int k_signed, int v_bits,
                        void* k_out, void* v_out, tq_dtype out_dtype, void* stream);
 
+/* Deferred-V decode (ops.ts: decodeValuesRotated, the deferV branch of
+ * tryDecodePackedKv). Same arguments, checks and K output as tq_decode_kv;
+ * v_out holds the values still in the rotated domain, centroid[idx] * scale
+ * per element (fp32 product of the centroid and the stored fp16 scale),
+ * rounded to out_dtype, with no inverse Hadamard transform and no signs.
+ * Attention over V is linear in V, so a caller may attend over these values
+ * and undo the rotation once per output row with tq_unrotate. */
+tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const void* k_zeros,
+                               const void* v_codes, const void* v_scales,
+                               int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
+                               int k_bits, int k_signed, int v_bits,
+                               void* k_out, void* v_out, tq_dtype out_dtype, void* stream);
+
+/* Inverse value rotation (ops.ts: unrotateValues, i.e. fwht(x, false)):
+ * for each of n_rows contiguous rows of D elements of type dtype, convert to
+ * fp32, apply the normalised Hadamard transform (ascending radix-2
+ * butterflies, then * fp32(1/sqrt(D))), multiply by the sign vector of D,
+ * and store in the same dtype. x and out are device pointers, 16-byte
+ * aligned, [n_rows, D], and must not overlap (the input is read through
+ * the read-only data path).
+ * D in {64,128,256,512}; n_rows == 0 is a no-op; n_rows < 2^31 - 64. */
+tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, void* out, void* stream);
+
 /* Lloyd-Max index (ops.ts, searchsorted): idx[i] = number of boundaries of
  * the v_bits table strictly below u[i] (NaN -> 0), for n fp32 values already
  * in the rotated, RMS-normalised domain. u and idx are device pointers

@@ -32,7 +32,8 @@ def _declared():
 
 def test_header_declares_the_abi():
     names = _declared()
-    for n in ("tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_lloyd_max_index", "tq_status_string"):
+    for n in ("tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated", "tq_unrotate",
+              "tq_lloyd_max_index", "tq_status_string"):
         assert n in names
 
 
@@ -69,7 +70,13 @@ def _dec(L, D=128, T=4, kb=8, ks=1, vb=3, dtype=1, t_cap=None, ptrs=None, B=1, H
     return L.tq_decode_kv(*ptrs[:5], B, H, T, D, t_cap, kb, ks, vb, ptrs[5], ptrs[6], dtype, None)
 
 
-@pytest.mark.parametrize("fn", [_enc, _dec])
+def _dec_rot(L, D=128, T=4, kb=8, ks=1, vb=3, dtype=1, t_cap=None, ptrs=None, B=1, H=2):
+    t_cap = T if t_cap is None else t_cap
+    ptrs = ptrs if ptrs is not None else [0] * 7
+    return L.tq_decode_kv_rotated(*ptrs[:5], B, H, T, D, t_cap, kb, ks, vb, ptrs[5], ptrs[6], dtype, None)
+
+
+@pytest.mark.parametrize("fn", [_enc, _dec, _dec_rot])
 def test_argument_checks(L, fn):
     assert fn(L, D=96) == HEAD_DIM and fn(L, D=32) == HEAD_DIM and fn(L, D=1024) == HEAD_DIM
     assert fn(L, vb=6) == BITS and fn(L, vb=1) == BITS
@@ -98,11 +105,24 @@ def test_misaligned_buffers_rejected(L):
         bad[i] += 8
         assert _enc(L, ptrs=bad) == ALIGN
         assert _dec(L, ptrs=bad) == ALIGN
+        assert _dec_rot(L, ptrs=bad) == ALIGN
 
 
 def test_size_overflow_rejected(L):
     assert _enc(L, B=1 << 20, H=1 << 20, T=1 << 12) == INVALID
     assert _dec(L, T=1 << 31, t_cap=1 << 31) == INVALID
+
+
+def test_unrotate_checks(L):
+    assert L.tq_unrotate(None, 1, 0, 128, None, None) == OK
+    assert L.tq_unrotate(None, 1, -1, 128, None, None) == INVALID
+    assert L.tq_unrotate(None, 1, 4, 96, None, None) == HEAD_DIM
+    assert L.tq_unrotate(None, 3, 4, 128, None, None) == DTYPE
+    assert L.tq_unrotate(None, 0, 4, 128, None, None) == INVALID
+    assert L.tq_unrotate(1 << 20, 0, 4, 128, None, None) == INVALID
+    assert L.tq_unrotate(1 << 20 | 8, 0, 4, 128, 1 << 21, None) == ALIGN
+    assert L.tq_unrotate(1 << 20, 0, 4, 128, (1 << 21) + 4, None) == ALIGN
+    assert L.tq_unrotate(1 << 20, 0, 1 << 31, 128, 1 << 21, None) == INVALID
 
 
 def test_lloyd_max_index_checks(L):

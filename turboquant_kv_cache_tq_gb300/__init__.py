@@ -18,7 +18,8 @@ import threading
 import torch
 
 __all__ = [
-    "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_lloyd_max_index",
+    "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated",
+    "tq_unrotate", "tq_lloyd_max_index",
     "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
 ]
 
@@ -62,6 +63,10 @@ def lib() -> ctypes.CDLL:
             L.tq_encode_kv.argtypes = [P, P, I, I64, I64, I64, I64, I, I, I, P, P, P, P, P, I64, I64, P]
             L.tq_decode_kv.restype = I
             L.tq_decode_kv.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
+            L.tq_decode_kv_rotated.restype = I
+            L.tq_decode_kv_rotated.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
+            L.tq_unrotate.restype = I
+            L.tq_unrotate.argtypes = [P, I, I64, I64, P, P]
             L.tq_lloyd_max_index.restype = I
             L.tq_lloyd_max_index.argtypes = [P, I64, I, P, P]
             L.tq_status_string.restype = ctypes.c_char_p
@@ -133,10 +138,7 @@ def tq_encode_kv(k: torch.Tensor, v: torch.Tensor, k_bits: int, k_signed: bool, 
     return cache
 
 
-def tq_decode_kv(cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
-                 out_dtype=torch.bfloat16, k_out=None, v_out=None, stream=None):
-    """Decode tokens [0,T) of `cache` into K, V [B,H,T,D] of `out_dtype`
-    (allocated when not given). Asynchronous on `stream`."""
+def _decode(fn, name, cache, T, k_bits, k_signed, v_bits, out_dtype, k_out, v_out, stream):
     B, H, t_cap, _ = cache["k_codes"].shape
     D = cache["k_scales"].shape[-1] * GROUP
     dev = cache["k_codes"].device
@@ -149,11 +151,43 @@ def tq_decode_kv(cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
     for t in (k_out, v_out):
         if t.dtype != out_dtype or tuple(t.shape) != (B, H, T, D) or not t.is_contiguous():
             raise ValueError("k_out/v_out must be contiguous [B,H,T,D] tensors of out_dtype")
-    st = lib().tq_decode_kv(*_cache_ptrs(cache), B, H, T, D, t_cap, int(k_bits), int(bool(k_signed)),
-                            int(v_bits), k_out.data_ptr(), v_out.data_ptr(), _DTYPE[out_dtype],
-                            _stream_handle(stream, dev))
-    _check(st, "tq_decode_kv")
+    st = fn(*_cache_ptrs(cache), B, H, T, D, t_cap, int(k_bits), int(bool(k_signed)), int(v_bits),
+            k_out.data_ptr(), v_out.data_ptr(), _DTYPE[out_dtype], _stream_handle(stream, dev))
+    _check(st, name)
     return k_out, v_out
+
+
+def tq_decode_kv(cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
+                 out_dtype=torch.bfloat16, k_out=None, v_out=None, stream=None):
+    """Decode tokens [0,T) of `cache` into K, V [B,H,T,D] of `out_dtype`
+    (allocated when not given). Asynchronous on `stream`."""
+    return _decode(lib().tq_decode_kv, "tq_decode_kv", cache, T, k_bits, k_signed, v_bits, out_dtype,
+                   k_out, v_out, stream)
+
+
+def tq_decode_kv_rotated(cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
+                         out_dtype=torch.bfloat16, k_out=None, v_out=None, stream=None):
+    """As tq_decode_kv, but V stays in the rotated domain (centroid * scale,
+    no inverse transform); undo it on an attention output with tq_unrotate."""
+    return _decode(lib().tq_decode_kv_rotated, "tq_decode_kv_rotated", cache, T, k_bits, k_signed, v_bits,
+                   out_dtype, k_out, v_out, stream)
+
+
+def tq_unrotate(x: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """Inverse value rotation of the rows of `x` ([..., D], fp32 or bf16,
+    contiguous), computed in fp32 and returned in x's dtype. `out` must not
+    overlap x."""
+    if x.dtype not in _DTYPE or not x.is_contiguous() or x.dim() < 1:
+        raise ValueError("x must be a contiguous float32 or bfloat16 tensor")
+    D = x.shape[-1]
+    if out is None:
+        out = torch.empty_like(x)
+    if out.dtype != x.dtype or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
+    n = x.numel() // D if D else 0
+    st = lib().tq_unrotate(x.data_ptr(), _DTYPE[x.dtype], n, D, out.data_ptr(), _stream_handle(stream, x.device))
+    _check(st, "tq_unrotate")
+    return out
 
 
 def tq_lloyd_max_index(u: torch.Tensor, v_bits: int, out=None, stream=None) -> torch.Tensor:

@@ -146,11 +146,13 @@ extern "C" tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtyp
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
-                                  const void* v_codes, const void* v_scales,
-                                  int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
-                                  int k_bits, int k_signed, int v_bits,
-                                  void* k_out, void* v_out, tq_dtype out_dtype, void* stream) {
+namespace tq {
+namespace {
+
+tq_status decode_impl(const void* k_codes, const void* k_scales, const void* k_zeros, const void* v_codes,
+                      const void* v_scales, int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap, int k_bits,
+                      int k_signed, int v_bits, void* k_out, void* v_out, tq_dtype out_dtype, bool rotated_v,
+                      void* stream) {
   long long rows = 0;
   const tq_status st = check_common(B, H, T, D, t_cap, 0, k_bits, k_signed, v_bits,
                                     static_cast<int>(out_dtype), &rows);
@@ -183,10 +185,56 @@ extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (D) {
-    case 64: e = launch_decode<64>(p, v_bits, bf16, s); break;
-    case 128: e = launch_decode<128>(p, v_bits, bf16, s); break;
-    case 256: e = launch_decode<256>(p, v_bits, bf16, s); break;
-    default: e = launch_decode<512>(p, v_bits, bf16, s); break;
+    case 64: e = launch_decode<64>(p, v_bits, bf16, rotated_v, s); break;
+    case 128: e = launch_decode<128>(p, v_bits, bf16, rotated_v, s); break;
+    case 256: e = launch_decode<256>(p, v_bits, bf16, rotated_v, s); break;
+    default: e = launch_decode<512>(p, v_bits, bf16, rotated_v, s); break;
+  }
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
+                                  const void* v_codes, const void* v_scales,
+                                  int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
+                                  int k_bits, int k_signed, int v_bits,
+                                  void* k_out, void* v_out, tq_dtype out_dtype, void* stream) {
+  return decode_impl(k_codes, k_scales, k_zeros, v_codes, v_scales, B, H, T, D, t_cap, k_bits, k_signed, v_bits,
+                     k_out, v_out, out_dtype, false, stream);
+}
+
+extern "C" tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const void* k_zeros,
+                                          const void* v_codes, const void* v_scales,
+                                          int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
+                                          int k_bits, int k_signed, int v_bits,
+                                          void* k_out, void* v_out, tq_dtype out_dtype, void* stream) {
+  return decode_impl(k_codes, k_scales, k_zeros, v_codes, v_scales, B, H, T, D, t_cap, k_bits, k_signed, v_bits,
+                     k_out, v_out, out_dtype, true, stream);
+}
+
+extern "C" tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, void* out, void* stream) {
+  if (n_rows < 0) return TQ_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return TQ_ERR_HEAD_DIM;
+  if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_DTYPE;
+  if (n_rows > 0x7fffffffLL - 64) return TQ_ERR_INVALID_ARG;
+  if (n_rows == 0) return TQ_OK;
+  if (!x || !out) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGNMENT;
+  UnrotateParams p{};
+  p.x = x;
+  p.out = out;
+  p.rows = static_cast<int>(n_rows);
+  p.rot_scale = rotation_scale(D);
+  const bool bf16 = dtype == TQ_BF16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_unrotate<64>(p, bf16, s); break;
+    case 128: e = launch_unrotate<128>(p, bf16, s); break;
+    case 256: e = launch_unrotate<256>(p, bf16, s); break;
+    default: e = launch_unrotate<512>(p, bf16, s); break;
   }
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

@@ -3,5 +3,6 @@
 #include "tq_kernels.cuh"
 
 namespace tq {
-template cudaError_t launch_decode<128>(const DecodeParams&, int, bool, cudaStream_t);
+template cudaError_t launch_decode<128>(const DecodeParams&, int, bool, bool, cudaStream_t);
+template cudaError_t launch_unrotate<128>(const UnrotateParams&, bool, cudaStream_t);
 }  // namespace tq

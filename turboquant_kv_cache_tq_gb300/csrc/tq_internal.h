@@ -53,11 +53,20 @@ struct DecodeParams {
   int ng;               // groups per row (D / 32)
 };
 
-// One launcher per head_dim (tq_kernels_d<D>.cu); v_bits in {2,3,4,5,8}.
+struct UnrotateParams {
+  const void* x;        // [rows, D] rotated values (fp32 or bf16)
+  void* out;            // [rows, D] same type
+  int rows;
+  float rot_scale;
+};
+
+// Launchers per head_dim (tq_encode_d<D>.cu, tq_decode_d<D>.cu); v_bits in {2,3,4,5,8}.
 template <int D>
 cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaStream_t s);
 template <int D>
-cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s);
+template <int D>
+cudaError_t launch_unrotate(const UnrotateParams& p, bool bf16, cudaStream_t s);
 
 cudaError_t launch_lloyd_max_index(const float* u, long long n, int v_bits, uint8_t* idx, cudaStream_t s);
 

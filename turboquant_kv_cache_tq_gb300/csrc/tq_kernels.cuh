@@ -398,7 +398,9 @@ __device__ __forceinline__ void store_group(void* base, size_t off, const float 
   }
 }
 
-template <int LPR, int VB, bool F32, int W, typename Prefetch>
+// V decode of one group. ROT: leave the values in the rotated domain
+// (dequantScaled / decodeValuesRotated: centroid * scale only).
+template <int LPR, int VB, bool F32, bool ROT, int W, typename Prefetch>
 __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, const uint32_t* s_sign,
                                                   const float* s_cent, float rot_scale, float neg_zero,
                                                   bool store, void* out, size_t out_off, Prefetch&& prefetch) {
@@ -415,12 +417,17 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
   prefetch();
 #pragma unroll
   for (int q = 0; q < 16; ++q) Y[q] = mul0(Y[q], f2(s), nz);  // feeds the butterflies: must stay rounded
-  hadamard_row<LPR>(Y, l);
-  const float2 c2 = f2(rot_scale);
-#pragma unroll
-  for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
   uint32_t S[16];
-  load_sign_words(s_sign, l, S);
+  if constexpr (ROT) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) S[j] = 0u;  // no signs in the rotated domain
+  } else {
+    hadamard_row<LPR>(Y, l);
+    const float2 c2 = f2(rot_scale);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
+    load_sign_words(s_sign, l, S);
+  }
   if (!store) return;
   if constexpr (!F32) {
     // round to bf16, then apply the signs on the packed words (exact)
@@ -443,7 +450,7 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
   }
 }
 
-template <int D, int VB, int KMODE, bool F32>
+template <int D, int VB, int KMODE, bool F32, bool ROT>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(DecodeParams p) {
   using G = Geo<D>;
   using M = KeySpec<KMODE>;
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
       decode_key_item<KMODE>(in, x, prefetch);
       if (valid) store_group<F32>(p.k_out, out_off, x);
     } else {
-      decode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cent, p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
+      decode_value_item<G::LPR, VB, F32, ROT>(in, l, s_sign, s_cent, p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
                                          prefetch);
     }
   }
@@ -535,11 +542,11 @@ cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int D, int VB, int KMODE, bool F32>
+template <int D, int VB, int KMODE, bool F32, bool ROT>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
-  static const int resident = resident_blocks(decode_kernel<D, VB, KMODE, F32>);
+  static const int resident = resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT>);
   const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
-  const cudaError_t e = launch_pdl(decode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s);
+  const cudaError_t e = launch_pdl(decode_kernel<D, VB, KMODE, F32, ROT>, grid_for(items, resident), p, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -554,14 +561,14 @@ cudaError_t launch_encode_vb(const EncodeParams& p, cudaStream_t s) {
   }
 }
 
-template <int D, int VB, bool F32>
+template <int D, int VB, bool F32, bool ROT>
 cudaError_t launch_decode_vb(const DecodeParams& p, cudaStream_t s) {
   switch (p.kmode) {
-    case kK2: return launch_decode_t<D, VB, kK2, F32>(p, s);
-    case kK4: return launch_decode_t<D, VB, kK4, F32>(p, s);
-    case kK5: return launch_decode_t<D, VB, kK5, F32>(p, s);
-    case kK8: return launch_decode_t<D, VB, kK8, F32>(p, s);
-    default: return launch_decode_t<D, VB, kK8Signed, F32>(p, s);
+    case kK2: return launch_decode_t<D, VB, kK2, F32, ROT>(p, s);
+    case kK4: return launch_decode_t<D, VB, kK4, F32, ROT>(p, s);
+    case kK5: return launch_decode_t<D, VB, kK5, F32, ROT>(p, s);
+    case kK8: return launch_decode_t<D, VB, kK8, F32, ROT>(p, s);
+    default: return launch_decode_t<D, VB, kK8Signed, F32, ROT>(p, s);
   }
 }
 
@@ -576,14 +583,14 @@ cudaError_t launch_encode_dt(const EncodeParams& p, int v_bits, cudaStream_t s) 
   }
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool ROT>
 cudaError_t launch_decode_dt(const DecodeParams& p, int v_bits, cudaStream_t s) {
   switch (v_bits) {
-    case 2: return launch_decode_vb<D, 2, F32>(p, s);
-    case 3: return launch_decode_vb<D, 3, F32>(p, s);
-    case 4: return launch_decode_vb<D, 4, F32>(p, s);
-    case 5: return launch_decode_vb<D, 5, F32>(p, s);
-    default: return launch_decode_vb<D, 8, F32>(p, s);
+    case 2: return launch_decode_vb<D, 2, F32, ROT>(p, s);
+    case 3: return launch_decode_vb<D, 3, F32, ROT>(p, s);
+    case 4: return launch_decode_vb<D, 4, F32, ROT>(p, s);
+    case 5: return launch_decode_vb<D, 5, F32, ROT>(p, s);
+    default: return launch_decode_vb<D, 8, F32, ROT>(p, s);
   }
 }
 
@@ -593,8 +600,73 @@ cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaS
 }
 
 template <int D>
-cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, cudaStream_t s) {
-  return out_bf16 ? launch_decode_dt<D, false>(p, v_bits, s) : launch_decode_dt<D, true>(p, v_bits, s);
+cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s) {
+  if (rotated_v)
+    return out_bf16 ? launch_decode_dt<D, false, true>(p, v_bits, s) : launch_decode_dt<D, true, true>(p, v_bits, s);
+  return out_bf16 ? launch_decode_dt<D, false, false>(p, v_bits, s) : launch_decode_dt<D, true, false>(p, v_bits, s);
+}
+
+// ---------------------------------------------------------------------------
+// unrotateValues: the inverse rotation (Hadamard transform, then signs) of
+// rows of D values in fp32 arithmetic, returned in the input's type. Same
+// lane layout as the codecs: lane l of a row owns elements [32l, 32l+32).
+template <int D, bool F32>
+__global__ void __launch_bounds__(kThreads) unrotate_kernel(UnrotateParams p) {
+  using G = Geo<D>;
+  __shared__ __align__(16) uint32_t s_sign[D / 2];
+  fill_sign_words<D>(s_sign);
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / G::LPR;
+  const int l = lane % G::LPR;
+  const int n_warps = gridDim.x * (blockDim.x >> 5);
+  const int tiles = (p.rows + G::RPW - 1) / G::RPW;
+  uint32_t S[16];
+  load_sign_words(s_sign, l, S);
+  for (int tile = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < tiles; tile += n_warps) {
+    const int r0 = tile * G::RPW + sub;
+    const bool valid = r0 < p.rows;
+    const size_t off = static_cast<size_t>(valid ? r0 : p.rows - 1) * D + kGroup * l;
+    ItemIn<F32> in;
+    load_item<F32>(p.x, off, in);
+    float2 Y[16];
+    item_to_pairs(in, Y);
+    hadamard_row<G::LPR>(Y, l);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], f2(p.rot_scale));
+    if (!valid) continue;
+    if constexpr (!F32) {
+      uint32_t o[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(Y[2 * j].x, Y[2 * j + 1].x);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(Y[2 * j].y, Y[2 * j + 1].y);
+        o[j] = *reinterpret_cast<const uint32_t*>(&a) ^ S[j];
+        o[j + 8] = *reinterpret_cast<const uint32_t*>(&b) ^ S[j + 8];
+      }
+      uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    } else {
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(S, i));
+      store_group<true>(p.out, off, x);
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_unrotate(const UnrotateParams& p, bool bf16, cudaStream_t s) {
+  const long long tiles = (p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW;
+  if (bf16) {
+    static const int resident = resident_blocks(unrotate_kernel<D, false>);
+    return launch_pdl(unrotate_kernel<D, false>, grid_for(tiles, resident), p, s);
+  }
+  static const int resident = resident_blocks(unrotate_kernel<D, true>);
+  return launch_pdl(unrotate_kernel<D, true>, grid_for(tiles, resident), p, s);
 }
 
 }  // namespace tq
