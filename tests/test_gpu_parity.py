@@ -149,10 +149,10 @@ def _key_groups(groups, D=64):
     return torch.from_numpy(g.copy()).view(1, 1, -1, D)
 
 
-def test_key_rounding_ties_take_the_exact_path():
+def test_key_rounding_ties():
     """Groups whose x / (scale + eps) - zero lands exactly on half-integers:
-    the fast quantisation must hand these to the exact path, which rounds
-    half to even like the page's round()."""
+    the quotient must be the correctly rounded one and round() half to even,
+    like the page's."""
     half = np.arange(32, dtype=np.float32) + np.float32(0.5)  # 5-bit: scale 1, zero 0, t = i + 0.5
     sym = np.concatenate([[-127.0, 127.0], np.arange(-15, 15) + 0.5]).astype(np.float32)  # int8: scale 1
     rows = [np.concatenate([half, half[::-1]]), np.concatenate([sym, -sym]),
@@ -161,6 +161,37 @@ def test_key_rounding_ties_take_the_exact_path():
     v = torch.from_numpy(np.random.default_rng(0).standard_normal(k.shape).astype(np.float32))
     for kb, ks in KEY_MODES:
         check_roundtrip(k, v, kb, ks, 3)
+
+
+@pytest.mark.parametrize("kb,ks", KEY_MODES)
+def test_key_quotient_rounding_stress(kb, ks):
+    """Groups on a power-of-two scale whose elements sit on, or one ulp
+    beside, half-integer multiples of the scale, and groups whose scale is
+    comparable to eps: every code depends on the exact rounding of
+    x / (scale + eps) and of the subtraction of the zero point."""
+    rng = np.random.default_rng(100 + kb + 10 * ks)
+    M = 127 if ks else (1 << kb) - 1
+    rows = []
+    for g in range(512):
+        e = int(rng.integers(-3, 12))
+        h = np.float32(2.0 ** e)
+        if ks:
+            base = rng.integers(-2 * M, 2 * M + 1, 32).astype(np.float32) * np.float32(0.5)
+            base[0], base[1] = -M, M
+        else:
+            base = rng.integers(0, 2 * M + 1, 32).astype(np.float32) * np.float32(0.5)
+            base[0], base[1] = 0, M
+        x = (base * h).astype(np.float32)
+        nudge = rng.integers(-1, 2, 32)
+        nudge[:2] = 0
+        x = np.where(nudge > 0, np.nextafter(x, np.float32(np.inf)),
+                     np.where(nudge < 0, np.nextafter(x, np.float32(-np.inf)), x)).astype(np.float32)
+        if g % 8 == 7:  # scale near eps: range ~ M * 1e-8
+            x = (rng.standard_normal(32) * M * 1e-8).astype(np.float32)
+        rows.append(rng.permutation(x))
+    k = _key_groups(np.concatenate(rows).reshape(-1, 64))
+    v = torch.from_numpy(np.random.default_rng(3).standard_normal(k.shape).astype(np.float32))
+    check_roundtrip(k, v, kb, ks, 3)
 
 
 def test_key_signed_zero_extremes():

@@ -216,7 +216,7 @@ __device__ __forceinline__ float group_sum_sq(const float2 (&P)[16], float2 nz) 
 // 1/S is below the table's smallest boundary gap), compared explicitly: u > b
 // exactly when RN(b - u) has its sign bit set. The grid covers |u| < 7.9; for
 // finite inputs |u| <= sqrt(32) since u is a coordinate over its group's RMS.
-struct CellEntry {
+struct __align__(8) CellEntry {  // one 64-bit shared-memory load
   float b;   // the boundary inside this cell, or +Inf
   int base;  // number of boundaries in lower cells
 };
@@ -322,15 +322,29 @@ __device__ __forceinline__ void lm_index2(float2 u, const CellEntry* tab, int& i
 // is RN(y * (inv * S) + magic) (inv * S is exact) and the comparison is the
 // sign of RN(b - y * inv) (one fma), so both use the same exact value
 // v = y * inv and the result is exactly count(boundaries < v).
-template <int BITS>
-__device__ __forceinline__ void lm_index2_scaled(float2 y, float inv, const CellEntry* tab, int& i0, int& i1) {
+// MASKED = false indexes the table by the float's bits minus the magic
+// constant's, without a mask: the caller guarantees |v| * S < OFF, which
+// holds whenever inv is the reciprocal of (a finite group RMS + eps) and y is
+// an element of that group (|y| <= sqrt(32) * rms, so |v * S| <= 5.66 S).
+// MASKED = true is safe for any input (NaN and Inf land in some cell).
+template <int BITS, bool MASKED>
+__device__ __forceinline__ void lm_index2_scaled(float2 y, float inv, const CellEntry* tab, uint32_t& i0,
+                                                 uint32_t& i1) {
   using G = CellGrid<BITS>;
   const float2 s = fma2(y, f2(__fmul_rn(inv, G::S)), f2(grid_magic<BITS>()));
-  const CellEntry e0 = tab[__float_as_uint(s.x) & (G::NC - 1)];
-  const CellEntry e1 = tab[__float_as_uint(s.y) & (G::NC - 1)];
+  uint32_t c0 = __float_as_uint(s.x), c1 = __float_as_uint(s.y);
+  if constexpr (MASKED) {
+    c0 &= G::NC - 1;
+    c1 &= G::NC - 1;
+  } else {
+    c0 -= kMagicBits;
+    c1 -= kMagicBits;
+  }
+  const CellEntry e0 = tab[c0];
+  const CellEntry e1 = tab[c1];
   const float2 d = fma2(y, f2(-inv), make_float2(e0.b, e1.b));
-  i0 = e0.base + static_cast<int>(__float_as_uint(d.x) >> 31);
-  i1 = e1.base + static_cast<int>(__float_as_uint(d.y) >> 31);
+  i0 = static_cast<uint32_t>(e0.base) + (__float_as_uint(d.x) >> 31);
+  i1 = static_cast<uint32_t>(e1.base) + (__float_as_uint(d.y) >> 31);
 }
 
 // Any fp32 value: clamp into the grid first (all boundaries lie inside it, so
@@ -373,6 +387,68 @@ __device__ __forceinline__ void put_code_exact(uint32_t (&w)[B], int i, uint32_t
   const int bit = i * B, word = bit >> 5, off = bit & 31;
   w[word] += v << off;
   if (off + B > 32) w[word + 1] += v >> (32 - off);
+}
+
+// Sum of (kMagicBits << offset) over the codes whose low part lies in word
+// `word`, modulo 2^32.
+template <int B>
+__host__ __device__ constexpr uint32_t magic_correction(int word) {
+  uint32_t c = 0;
+  for (int i = 0; i < 32; ++i) {
+    const int bit = i * B;
+    if ((bit >> 5) == word) c += kMagicBits << (bit & 31);
+  }
+  return c;
+}
+
+// Low bytes of four words, in order, as one word.
+__device__ __forceinline__ uint32_t gather_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Pack the 32 codes of a group, produced pair by pair: code_pair(q, lo, hi)
+// yields the codes of elements q and q + 16 (the pair layout). Code i goes
+// to bits [i*B, i*B+B) of w.
+//   MAGIC = false: codes are plain values in [0, 2^B).
+//   MAGIC = true: codes are float bit patterns kMagicBits + code (the output
+//     of rounding by the magic constant), code in [0, 2^B), or in
+//     [-127, 127] for B = 8. Narrow codes are accumulated shifted, pattern
+//     and all, and the magic constant's share of each word is subtracted once
+//     at the end (exact modulo 2^32); the part of a code that spills into the
+//     next word is its true value shifted down.
+// B = 8 takes the low byte of each code (two's complement when negative),
+// four codes per word with byte permutes.
+template <int B, bool MAGIC, typename CodePair>
+__device__ __forceinline__ void pack_pairs(uint32_t (&w)[B], CodePair&& code_pair) {
+  if constexpr (B == 8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) code_pair(4 * j + r, lo[r], hi[r]);
+      w[j] = gather_low_bytes(lo[0], lo[1], lo[2], lo[3]);
+      w[j + 4] = gather_low_bytes(hi[0], hi[1], hi[2], hi[3]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] = 0;
+    auto put = [&](int i, uint32_t c) {
+      const int bit = i * B, word = bit >> 5, off = bit & 31;
+      w[word] += c << off;
+      if (off + B > 32) w[word + 1] += (MAGIC ? c - kMagicBits : c) >> (32 - off);
+    };
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      uint32_t lo, hi;
+      code_pair(q, lo, hi);
+      put(q, lo);
+      put(q + 16, hi);
+    }
+    if constexpr (MAGIC) {
+#pragma unroll
+      for (int k = 0; k < B; ++k) w[k] -= magic_correction<B>(k);
+    }
+  }
 }
 
 template <int B>

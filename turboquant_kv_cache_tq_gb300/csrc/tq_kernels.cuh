@@ -12,11 +12,11 @@
 //   centroid * scale, Hadamard transform, signs for V (decodeValues).
 //
 // Division-free quantisation:
-//   K: t = RN(x * RN(1/se) - zp) differs from the page's RN(RN(x / se) - zp)
-//      by at most (|x/se| + |zp|) * 2^-22 (four unit roundoffs), so whenever t
-//      is farther than that from a half-integer both round to the same code.
-//      A lane whose group has any element inside that band recomputes the
-//      group with IEEE division; K codes are therefore exactly the page's.
+//   K: RN(x / se) is obtained exactly from the reciprocal by one correction
+//      step (q0 = RN(x * RN(1/se)), r = x - q0 * se exact, q = RN(q0 + r *
+//      RN(1/se))), then RN(q - zp) and rint, the page's operations in order,
+//      so K codes are exactly the page's. A warp with a group whose codes
+//      need the clamp (or whose quotient could overflow) takes IEEE division.
 //   V: the index is count(boundaries < v) for the exact product
 //      v = y * RN(1/se), which is within one ulp of RN(y / se) (|v| <=
 //      sqrt(32), so within 5e-7); it can only differ from the divided value's
@@ -122,8 +122,8 @@ __device__ __forceinline__ void item_to_pairs(const ItemIn<F32>& in, float2 (&P)
 // K encode of the group held by this lane. `prefetch` runs once the inputs
 // are in registers (it may overwrite `in`).
 template <int KMODE, bool F32, typename Prefetch>
-__device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, bool store, uint8_t* codes, uint16_t* scale_out,
-                                                uint16_t* zero_out, Prefetch&& prefetch) {
+__device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero, bool store, uint8_t* codes,
+                                                uint16_t* scale_out, uint16_t* zero_out, Prefetch&& prefetch) {
   using M = KeySpec<KMODE>;
   float2 X[16];
   float mn, mx;
@@ -164,47 +164,41 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, bool store, uin
   }
   const float se = __fadd_rn(scale, kEps);
   const float inv = __frcp_rn(se);
-  // guard band: (max|x| * inv + |zp|) * 2.5e-7 >= the fast/exact gap bound
-  const float amax = fmaxf(fabsf(mn), fabsf(mx));
-  const float band = __fmul_rn(__fadd_rn(__fmul_rn(amax, inv), fabsf(zp)), 2.5e-7f);
-  const float thr = __fsub_rn(0.5f, band);
+  const float2 nz = f2(neg_zero);
+  // Code of a pair as the float bit pattern kMagicBits + rint(RN(RN(x/se) - zp)).
+  // RN(x/se) exactly by one correction step: with inv = RN(1/se) and
+  // q0 = RN(x * inv) (within an ulp of x/se), the remainder r = x - q0 * se is
+  // exact and RN(q0 + r * inv) is the correctly rounded quotient, barring
+  // overflow of x/se (the caller's range test rejects it) and underflow of r
+  // (only when |x/se| < 2^-70, too small to move rint(q - zp)).
+  auto code_bits = [&](float2 x) {
+    const float2 q0 = mul0(x, f2(inv), nz);  // rounded: it is the quotient's first guess
+    const float2 r = fma2(q0, f2(-se), x);
+    const float2 q = fma2(r, f2(inv), q0);
+    return add2(add2(q, f2(-zp)), f2(kMagic));  // RN(q - zp), then rint
+  };
   const int lo_bits = static_cast<int>(kMagicBits) + M::kLo;
   const int hi_bits = static_cast<int>(kMagicBits) + M::kHi;
-  // t = RN(x * inv - zp) is monotone in x, so when the group's min and max
-  // round inside the code range every element does and no clamp is needed.
-  const float2 ext = add2(fma2(make_float2(mn, mx), f2(inv), f2(-zp)), f2(kMagic));
+  // The code is monotone in x, so when the group's min and max have codes
+  // inside [kLo, kHi] every element does and no clamp is needed (an
+  // overflowed quotient gives NaN or Inf, which fails this test).
+  const float2 ext = code_bits(make_float2(mn, mx));
   const bool in_range = __float_as_int(ext.x) >= lo_bits && __float_as_int(ext.y) <= hi_bits;
 
   uint32_t w[M::B];
-#pragma unroll
-  for (int k = 0; k < M::B; ++k) w[k] = 0;
-  bool ok = true;
   if (__all_sync(kFull, in_range)) {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float2 t = fma2(X[q], f2(inv), f2(-zp));
-      const float2 s = add2(t, f2(kMagic));
-      const float2 d = sub2(t, sub2(s, f2(kMagic)));
-      ok = ok && (fabsf(d.x) < thr) && (fabsf(d.y) < thr);
-      put_code<M::B>(w, q, static_cast<uint32_t>(__float_as_int(s.x)));
-      put_code<M::B>(w, q + 16, static_cast<uint32_t>(__float_as_int(s.y)));
-    }
+    pack_pairs<M::B, true>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
+      const float2 c = code_bits(X[q]);
+      lo = __float_as_uint(c.x);
+      hi = __float_as_uint(c.y);
+    });
   } else {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float2 t = fma2(X[q], f2(inv), f2(-zp));
-      const float2 s = add2(t, f2(kMagic));
-      const float2 d = sub2(t, sub2(s, f2(kMagic)));
-      ok = ok && (fabsf(d.x) < thr) && (fabsf(d.y) < thr);
-      put_code<M::B>(w, q, static_cast<uint32_t>(min(max(__float_as_int(s.x), lo_bits), hi_bits)));
-      put_code<M::B>(w, q + 16, static_cast<uint32_t>(min(max(__float_as_int(s.y), lo_bits), hi_bits)));
-    }
-  }
-  if (!ok) {  // rare: an element within the guard band of a rounding tie
-#pragma unroll
-    for (int k = 0; k < M::B; ++k) w[k] = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) put_code<M::B>(w, i, key_code_exact<KMODE>(pair_elem(X, i), se, zp));
+    // rare: some group of the warp needs the clamp: the page's operations
+    // with IEEE division, element by element
+    pack_pairs<M::B, true>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
+      lo = kMagicBits + key_code_exact<KMODE>(X[q].x, se, zp);
+      hi = kMagicBits + key_code_exact<KMODE>(X[q].y, se, zp);
+    });
   }
   if (store) {
     store_words<M::B>(codes, w);
@@ -238,14 +232,15 @@ __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const 
   const float rms = __fsqrt_rn(__fmul_rn(group_sum_sq(Y, f2(neg_zero)), 1.0f / kGroup));  // /32 is exact
   const float inv = __frcp_rn(__fadd_rn(rms, kEps));
   uint32_t w[VB];
-#pragma unroll
-  for (int k = 0; k < VB; ++k) w[k] = 0;
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    int i0, i1;
-    lm_index2_scaled<VB>(Y[q], inv, s_cells, i0, i1);
-    put_code<VB>(w, q, static_cast<uint32_t>(i0));
-    put_code<VB>(w, q + 16, static_cast<uint32_t>(i1));
+  if (__all_sync(kFull, __float_as_uint(rms) < 0x7f800000u)) {
+    // every group of the warp has a finite RMS: cells are in range unmasked
+    pack_pairs<VB, false>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
+      lm_index2_scaled<VB, false>(Y[q], inv, s_cells, lo, hi);
+    });
+  } else {
+    pack_pairs<VB, false>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
+      lm_index2_scaled<VB, true>(Y[q], inv, s_cells, lo, hi);
+    });
   }
   if (store) {
     store_words<VB>(codes, w);
@@ -306,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(Enco
       }
     };
     if (!is_v) {
-      encode_key_item<KMODE, F32>(in, valid, p.k_codes + orow * pdk + 4 * M::B * l, p.k_scales + orow * NG + l,
+      encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l, p.k_scales + orow * NG + l,
                                   p.k_zeros + orow * NG + l, prefetch);
     } else {
       encode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cells, p.rot_scale, p.neg_zero, valid,
