@@ -26,9 +26,10 @@
 // Geo<D>::RPW rows. Item `it` maps to tile it/2, and a warp alternates kinds
 // from one grid-stride step to the next (kind = (it ^ step) & 1, a bijection
 // because the number of warps is even), so registers cover one half at a time
-// and blocks stay balanced. The next item's inputs are loaded before the
-// current item's math. Lanes of a partial last tile redo the last row (so
-// shuffles stay converged) but store nothing.
+// and blocks stay balanced. Encode streams its inputs through a per-warp
+// shared-memory ring (EncodeRing), several items ahead; decode loads the next
+// item's packed words before the current item's math. Lanes of a partial last
+// tile redo the last row (so shuffles stay converged) but store nothing.
 //
 // Launch: the kernels are launched with programmatic stream serialization.
 // A block fills its shared tables, lets dependent launches begin
@@ -54,6 +55,37 @@ constexpr int kDecodeMinBlocks = TQ_DECODE_MIN_BLOCKS;
 
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Encode input staging: each warp streams its items' inputs through a ring of
+// shared-memory stages filled by asynchronous 16-byte copies (cp.async), so a
+// warp keeps several items' loads in flight without holding them in
+// registers. A lane copies, and later reads back, only its own group: the
+// copies of one lane complete and become visible to that lane at
+// cp.async.wait_group, so no cross-lane synchronisation is needed. Within a
+// stage, lane L's 16-byte chunk j sits at chunk (j xor swz(L)), which keeps
+// the 128-bit reads of every quarter-warp on distinct banks.
+#ifndef TQ_ENCODE_STAGES
+#define TQ_ENCODE_STAGES 4
+#endif
+template <bool F32>
+struct EncodeRing {
+  static constexpr int kLaneBytes = F32 ? 128 : 64;  // 32 inputs
+  static constexpr int kChunks = kLaneBytes / 16;
+  static constexpr int kStages = F32 ? 2 : TQ_ENCODE_STAGES;  // a power of two
+  static constexpr int kStageBytes = 32 * kLaneBytes;
+  static constexpr int kBlockBytes = (kThreads / 32) * kStages * kStageBytes;
+  static_assert((kStages & (kStages - 1)) == 0, "stages must be a power of two");
+  __device__ static int swz(int lane) { return F32 ? (lane & 7) : ((lane >> 1) & 3); }
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 template <int KMODE>
 struct KeySpec {
@@ -277,37 +309,57 @@ __global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(Enco
 
   // item -> row of this lane (clamped to the last row for a partial tile)
   auto item_row = [&](int it) { const int r0 = (it >> 1) * G::RPW + sub; return r0 < p.rows ? r0 : p.rows - 1; };
-  ItemIn<F32> in;
-  int step = 0;
-  if (gw < items) {
-    const bool v0 = ((gw ^ step) & 1) != 0;
-    load_item<F32>(v0 ? p.v : p.k, static_cast<size_t>(item_row(gw)) * D + kGroup * l, in);
-  }
-  for (int it = gw; it < items; it += n_warps, ++step) {
-    const bool is_v = ((it ^ step) & 1) != 0;
+  using R = EncodeRing<F32>;
+  extern __shared__ __align__(128) uint8_t s_ring[];
+  uint8_t* lane_ring = s_ring + (threadIdx.x >> 5) * (R::kStages * R::kStageBytes) + lane * R::kLaneBytes;
+  const uint32_t lane_ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(lane_ring));
+  const int swz = R::swz(lane);
+  // Step k of this warp handles item gw + k * n_warps, of kind (item ^ k) & 1,
+  // staged in slot k mod kStages. Every step commits one copy group (empty
+  // past the end), so wait_group(kStages - 1) always means "step k landed".
+  auto issue = [&](int it, int k) {
+    if (it < items) {
+      const bool v = ((it ^ k) & 1) != 0;
+      const char* src = static_cast<const char*>(v ? p.v : p.k) +
+                        (static_cast<size_t>(item_row(it)) * D + kGroup * l) * (F32 ? 4 : 2);
+      const uint32_t dst = lane_ring_sh + (k & (R::kStages - 1)) * R::kStageBytes;
+#pragma unroll
+      for (int j = 0; j < R::kChunks; ++j) cp_async16(dst + 16 * (j ^ swz), src + 16 * j);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < R::kStages - 1; ++k) issue(gw + k * n_warps, k);
+  auto no_prefetch = [] {};
+  int k = 0;
+  for (int it = gw; it < items; it += n_warps, ++k) {
+    issue(it + (R::kStages - 1) * n_warps, k + R::kStages - 1);
+    cp_async_wait<R::kStages - 1>();
+    ItemIn<F32> in;
+    {
+      const uint8_t* slot = lane_ring + (k & (R::kStages - 1)) * R::kStageBytes;
+#pragma unroll
+      for (int j = 0; j < R::kChunks; ++j) {
+        const uint4 u = *reinterpret_cast<const uint4*>(slot + 16 * (j ^ swz));
+        in.w[4 * j] = u.x; in.w[4 * j + 1] = u.y; in.w[4 * j + 2] = u.z; in.w[4 * j + 3] = u.w;
+      }
+    }
+    const bool is_v = ((it ^ k) & 1) != 0;
     const int r0 = (it >> 1) * G::RPW + sub;
     const bool valid = r0 < p.rows;
     const int r = valid ? r0 : p.rows - 1;
     const int bh = fast_div(r, p.tdiv);
     const long long orow = static_cast<long long>(bh) * p.t_cap + p.t_off + (r - bh * p.T);
-
-    const int nx = it + n_warps;
-    // the next item's loads are issued once this item's inputs are converted,
-    // so they overlap this item's math
-    auto prefetch = [&]() {
-      if (nx < items) {
-        const bool nv = ((nx ^ (step + 1)) & 1) != 0;
-        load_item<F32>(nv ? p.v : p.k, static_cast<size_t>(item_row(nx)) * D + kGroup * l, in);
-      }
-    };
     if (!is_v) {
-      encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l, p.k_scales + orow * NG + l,
-                                  p.k_zeros + orow * NG + l, prefetch);
+      encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l,
+                                  p.k_scales + orow * NG + l, p.k_zeros + orow * NG + l, no_prefetch);
     } else {
       encode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cells, p.rot_scale, p.neg_zero, valid,
-                                         p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l, prefetch);
+                                         p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l,
+                                         no_prefetch);
     }
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -501,11 +553,20 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
 
 // ---------------------------------------------------------------------------
 template <typename K>
-inline int resident_blocks(K kernel) {
+inline int resident_blocks(K kernel, int dyn_smem = 0) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, dyn_smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   return per_sm * sm_count();
+}
+
+// Opt a kernel into dynamic shared memory above the default limit, with the
+// largest shared-memory carveout; returns its resident blocks on the device.
+template <typename K>
+inline int prepare_dyn_smem(K kernel, int dyn_smem) {
+  cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  return resident_blocks(kernel, dyn_smem);
 }
 
 inline int grid_for(long long items, int resident) {
@@ -515,11 +576,11 @@ inline int grid_for(long long items, int resident) {
 
 // Launch with programmatic stream serialization (see the file comment).
 template <typename Params>
-inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p, cudaStream_t s) {
+inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p, cudaStream_t s, int dyn_smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -531,9 +592,10 @@ inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p,
 
 template <int D, int VB, int KMODE, bool F32>
 cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
-  static const int resident = resident_blocks(encode_kernel<D, VB, KMODE, F32>);
+  constexpr int smem = EncodeRing<F32>::kBlockBytes;
+  static const int resident = prepare_dyn_smem(encode_kernel<D, VB, KMODE, F32>, smem);
   const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
-  const cudaError_t e = launch_pdl(encode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s);
+  const cudaError_t e = launch_pdl(encode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s, smem);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
