@@ -87,6 +87,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Global warp index, numbered across blocks first (warp w of block b is
+// w * gridDim.x + b), so that when the items do not divide evenly the warps
+// with one item more are spread over all blocks, hence over all SMs.
+__device__ __forceinline__ int warp_index() { return static_cast<int>((threadIdx.x >> 5) * gridDim.x + blockIdx.x); }
+
 template <int KMODE>
 struct KeySpec {
   static constexpr int B = (KMODE == kK2) ? 2 : (KMODE == kK4) ? 4 : (KMODE == kK5) ? 5 : 8;
@@ -184,18 +189,35 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
   prefetch();
   if (mn == 0.0f || mx == 0.0f) scan_min_max(X, mn, mx);
 
+  // The group's quotients by the reciprocal and one remainder correction
+  // (see code_bits below). scale = RN(range / levels): exact for every finite
+  // range >= 2^-100 (checked exhaustively on the host for all five level
+  // counts); below that it can be an ulp off, which changes neither
+  // RN(scale + eps) (= eps) nor the fp16 scale (0). Inf and NaN ranges keep
+  // IEEE semantics through the plain product.
+  constexpr float kLevels = static_cast<float>(M::SIGNED ? 2 * M::kMax : M::kMax);
+  constexpr float kInvLevels = 1.0f / kLevels;
   const float range = __fsub_rn(mx, mn);
-  float scale, zp;
-  if constexpr (M::SIGNED) {
-    scale = __fdiv_rn(range, static_cast<float>(2 * M::kMax));
-    const float denom = __fmul_rn(2.0f, __fadd_rn(scale, kEps));
-    zp = rintf(__fdiv_rn(__fadd_rn(mx, mn), denom));
-  } else {
-    scale = __fdiv_rn(range, static_cast<float>(M::kMax));
-    zp = rintf(__fdiv_rn(mn, __fadd_rn(scale, kEps)));
-  }
+  const float sq0 = __fmul_rn(range, kInvLevels);
+  const float scale =
+      range <= 3.402823466e38f ? __fmaf_rn(__fmaf_rn(-sq0, kLevels, range), kInvLevels, sq0) : sq0;
   const float se = __fadd_rn(scale, kEps);
   const float inv = __frcp_rn(se);
+  // zero point: RN(mn / se), or RN((mx + mn) / (2 se)) = RN((mx + mn) / se) / 2
+  // for signed keys; a quotient that overflows takes IEEE division. The
+  // corrected quotient takes the sign of num (se > 0): for num = -0 the
+  // correction's exact zero remainder would otherwise turn -0 into +0, and
+  // the fp16 zero point keeps that sign.
+  const float num = M::SIGNED ? __fadd_rn(mx, mn) : mn;
+  const float zq0 = __fmul_rn(num, inv);
+  float zq;
+  if (fabsf(zq0) <= 3.402823466e38f) {
+    zq = copysignf(__fmaf_rn(__fmaf_rn(-zq0, se, num), inv, zq0), num);
+    if constexpr (M::SIGNED) zq = __fmul_rn(zq, 0.5f);
+  } else {
+    zq = M::SIGNED ? __fdiv_rn(num, __fmul_rn(2.0f, se)) : __fdiv_rn(num, se);
+  }
+  const float zp = rintf(zq);
   const float2 nz = f2(neg_zero);
   // Code of a pair as the float bit pattern kMagicBits + rint(RN(RN(x/se) - zp)).
   // RN(x/se) exactly by one correction step: with inv = RN(1/se) and
@@ -305,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(Enco
   const int n_warps = gridDim.x * (blockDim.x >> 5);
   const int tiles = (p.rows + G::RPW - 1) / G::RPW;
   const int items = 2 * tiles;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int gw = warp_index();
 
   // item -> row of this lane (clamped to the last row for a partial tile)
   auto item_row = [&](int it) { const int r0 = (it >> 1) * G::RPW + sub; return r0 < p.rows ? r0 : p.rows - 1; };
@@ -394,33 +416,41 @@ __device__ __forceinline__ void load_packed_item(const DecodeParams& p, bool is_
 // K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
 // Codes become floats through the 1.5 * 2^23 encoding (exact for |q| < 2^22).
 // `prefetch` runs once the packed inputs are consumed (it may overwrite `in`).
+// K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
+// Each code becomes the float 1.5 * 2^23 + bias + code (bias = 128 for
+// signed codes, whose bytes are first offset to [1, 255] by flipping their
+// sign bits), built directly as a bit pattern: a byte permute for 8-bit
+// codes, a shift and a mask otherwise. The zero point is an integer (or
+// +-Inf, or NaN), so zero - 1.5 * 2^23 - bias is exact and adding it to that
+// float gives RN(code + zero) in one rounding, as the page's sum does.
+// `prefetch` runs once the packed inputs are consumed (it may overwrite `in`).
 template <int KMODE, int W, typename Prefetch>
 __device__ __forceinline__ void decode_key_item(const PackedIn<W>& in, float (&x)[32], Prefetch&& prefetch) {
   using M = KeySpec<KMODE>;
+  constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
   const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz & 0xffffu)));
   const float z = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz >> 16)));
-  float2 f[16];
-  {
+  const float zb = __fsub_rn(z, kBias);
+  uint32_t cb[32];
+  if constexpr (M::B == 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t wk = M::SIGNED ? (in.w[k] ^ 0x80808080u) : in.w[k];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cb[4 * k + j] = __byte_perm(wk, kMagicBits, 0x7640u | j);
+    }
+  } else {
     uint32_t w[M::B];
 #pragma unroll
     for (int k = 0; k < M::B; ++k) w[k] = in.w[k];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      int q0 = static_cast<int>(unpack_code<M::B>(w, i));
-      int q1 = static_cast<int>(unpack_code<M::B>(w, i + 1));
-      if constexpr (M::SIGNED) {
-        q0 = static_cast<int>(static_cast<int8_t>(q0));
-        q1 = static_cast<int>(static_cast<int8_t>(q1));
-      }
-      f[i / 2] = make_float2(__int_as_float(static_cast<int>(kMagicBits) + q0),
-                             __int_as_float(static_cast<int>(kMagicBits) + q1));
-    }
+    for (int i = 0; i < 32; ++i) cb[i] = unpack_code<M::B>(w, i) | kMagicBits;
   }
   prefetch();
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float2 g = sub2(f[i], f2(kMagic));   // the code, exactly
-    g = mul2(add2(g, f2(z)), f2(s));     // (code + zero) * scale
+    const float2 f = make_float2(__uint_as_float(cb[2 * i]), __uint_as_float(cb[2 * i + 1]));
+    const float2 g = mul2(add2(f, f2(zb)), f2(s));  // RN(RN(code + zero) * scale)
     x[2 * i] = g.x;
     x[2 * i + 1] = g.y;
   }
@@ -445,6 +475,41 @@ __device__ __forceinline__ void store_group(void* base, size_t off, const float 
   }
 }
 
+// Centroid tables in shared memory. 8-bit codes index 256 entries, which 32
+// lanes would hit with bank conflicts, so that table is kept once per bank:
+// entry c for lane L at word 32 c + L (s_cent is then offset by the lane).
+// Smaller tables (<= 32 entries) map every entry to its own bank already.
+template <int VB>
+struct CentroidTable {
+  static constexpr int kRep = VB == 8 ? 32 : 1;
+  static constexpr int kWords = (1 << VB) * kRep;
+};
+
+template <int VB>
+__device__ __forceinline__ void fill_centroids(float* s_cent) {
+  constexpr int rep = CentroidTable<VB>::kRep;
+  for (int i = threadIdx.x; i < CentroidTable<VB>::kWords; i += blockDim.x) s_cent[i] = centroid_table<VB>()[i / rep];
+}
+
+// Centroid of code i of the group, read at a byte offset formed straight from
+// the packed words (shift and mask; codes straddling two words are unpacked
+// first). `cent` is the table, already offset by the lane when replicated.
+template <int VB>
+__device__ __forceinline__ float centroid_at(const float* cent, const uint32_t (&w)[VB], int i) {
+  constexpr int kShift = VB == 8 ? 7 : 2;  // bytes per code step: 128 when replicated, else 4
+  constexpr uint32_t kMask = ((1u << VB) - 1u) << kShift;
+  const int bit = i * VB, word = bit >> 5, off = bit & 31;
+  uint32_t byte_off;
+  if (off + VB > 32) {
+    byte_off = unpack_code<VB>(w, i) << kShift;
+  } else if (off >= kShift) {
+    byte_off = (w[word] >> (off - kShift)) & kMask;
+  } else {
+    byte_off = (w[word] << (kShift - off)) & kMask;
+  }
+  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(cent) + byte_off);
+}
+
 // V decode of one group. ROT: leave the values in the rotated domain
 // (dequantScaled / decodeValuesRotated: centroid * scale only).
 template <int LPR, int VB, bool F32, bool ROT, int W, typename Prefetch>
@@ -459,7 +524,7 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
 #pragma unroll
     for (int k = 0; k < VB; ++k) w[k] = in.w[k];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) Y[q] = make_float2(s_cent[unpack_code<VB>(w, q)], s_cent[unpack_code<VB>(w, q + 16)]);
+    for (int q = 0; q < 16; ++q) Y[q] = make_float2(centroid_at<VB>(s_cent, w, q), centroid_at<VB>(s_cent, w, q + 16));
   }
   prefetch();
 #pragma unroll
@@ -501,11 +566,10 @@ template <int D, int VB, int KMODE, bool F32, bool ROT>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(DecodeParams p) {
   using G = Geo<D>;
   using M = KeySpec<KMODE>;
-  constexpr int NCENT = 1 << VB;
   constexpr int W = M::B > VB ? M::B : VB;
-  __shared__ float s_cent[NCENT];
+  __shared__ float s_cent[CentroidTable<VB>::kWords];
   __shared__ __align__(16) uint32_t s_sign[D / 2];
-  for (int i = threadIdx.x; i < NCENT; i += blockDim.x) s_cent[i] = centroid_table<VB>()[i];
+  fill_centroids<VB>(s_cent);
   fill_sign_words<D>(s_sign);
   __syncthreads();
   pdl_launch_dependents();
@@ -517,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
   const int n_warps = gridDim.x * (blockDim.x >> 5);
   const int tiles = (p.rows + G::RPW - 1) / G::RPW;
   const int items = 2 * tiles;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int gw = warp_index();
 
   auto item_irow = [&](int it) {
     const int r0 = (it >> 1) * G::RPW + sub;
@@ -545,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
       decode_key_item<KMODE>(in, x, prefetch);
       if (valid) store_group<F32>(p.k_out, out_off, x);
     } else {
-      decode_value_item<G::LPR, VB, F32, ROT>(in, l, s_sign, s_cent, p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
+      decode_value_item<G::LPR, VB, F32, ROT>(in, l, s_sign, s_cent + (CentroidTable<VB>::kRep > 1 ? lane : 0),
+                                              p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
                                          prefetch);
     }
   }
