@@ -17,7 +17,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SOURCES = ("tq_oracle.c", "tq_oracle_tables.c")
+_SOURCES = ("tq_oracle.c", "tq_oracle_tables.c", "tq_oracle_attention.c")
 LIB_PATH = os.path.join(_HERE, "libtq_oracle.so")
 CFLAGS = ("-O2", "-std=c11", "-Wall", "-Wextra", "-ffp-contract=off", "-fno-fast-math", "-fPIC")
 
@@ -84,6 +84,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_encode_kv": (I, [P, P, I, I64, I64, I64, I64, I, I, I, P, P, P, P, P, I64, I64]),
         "oracle_decode_kv": (I, [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, I]),
         "oracle_unrotate_rows": (I, [P, I64, I, P]),
+        "oracle_decode_attention": (I, [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P,
+                                        ctypes.c_double, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -323,3 +325,29 @@ def decode_kv(cache, T: int, k_bits: int, k_signed: bool, v_bits: int, out_dtype
                                 int(rotated_v))
     _check(st, "decode_kv")
     return ko, vo
+
+
+def decode_attention(q_bits, cache, T: int, k_bits: int, k_signed: bool, v_bits: int,
+                     left_pad=None, scale=None) -> np.ndarray:
+    """Attention of bf16 queries q [B,Hq,Nq,D] (uint16 bit patterns) over tokens
+    [0,T) of a packed cache (tryDecodePackedKv with deferV, softmax attention,
+    unrotateValues), in double precision -> float64 [B,Hq,Nq,D]."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    B, Hq, Nq, D = q_bits.shape
+    Bc, Hkv, t_cap, _ = cache["k_codes"].shape
+    if Bc != B:
+        raise OracleError("q and cache batch differ")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    lp = None
+    if left_pad is not None:
+        lp = np.ascontiguousarray(left_pad, dtype=np.int32)
+        if lp.shape != (B,):
+            raise OracleError("left_pad must have one entry per batch row")
+    out = np.empty((B, Hq, Nq, D), np.float64)
+    st = lib().oracle_decode_attention(_ptr(q_bits), B, Hq, Nq, _ptr(cache["k_codes"]), _ptr(cache["k_scales"]),
+                                       _ptr(cache["k_zeros"]), _ptr(cache["v_codes"]), _ptr(cache["v_scales"]),
+                                       Hkv, T, D, t_cap, k_bits, int(k_signed), v_bits,
+                                       None if lp is None else _ptr(lp), float(scale), _ptr(out))
+    _check(st, "decode_attention")
+    return out

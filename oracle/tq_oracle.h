@@ -144,6 +144,19 @@ int oracle_decode_kv(const uint8_t* k_codes, const uint16_t* k_scales, const uin
 /* unrotateValues: inverse rotation of n rows of d values (fp32 in, fp32 out). */
 int oracle_unrotate_rows(const float* x, int64_t n, int d, float* out);
 
+/* ---- decode attention over a packed cache (tq_oracle_attention.c) ----- */
+/* q: [B,Hq,Nq,D] bf16 bit patterns; cache: [B,Hkv,t_cap,X], tokens [0,T)
+ * valid; left_pad: B entries or NULL; out: [B,Hq,Nq,D] doubles, the attention
+ * output after the inverse rotation. Query head hq reads kv head hq/(Hq/Hkv);
+ * query token n attends to keys left_pad[b] <= t <= T-Nq+n; a row with no
+ * valid key is zero. */
+int oracle_decode_attention(const uint16_t* q, int64_t B, int64_t Hq, int64_t Nq,
+                            const uint8_t* k_codes, const uint16_t* k_scales, const uint16_t* k_zeros,
+                            const uint8_t* v_codes, const uint16_t* v_scales,
+                            int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
+                            int k_bits, int k_signed, int v_bits,
+                            const int32_t* left_pad, double scale, double* out);
+
 #ifdef __cplusplus
 }
 #endif
