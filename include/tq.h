@@ -116,6 +116,49 @@ tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, 
  * encode kernel uses. */
 tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx, void* stream);
 
+/* Fused decode attention over a packed cache (ops.ts: the deferV branch of
+ * tryDecodePackedKv, i.e. decodeKeys and decodeValuesRotated returning bf16,
+ * attention over those rows, then unrotateValues on the output; the left-pad
+ * key mask of batched decode, batched-mask.ts). The decoded cache is never
+ * written to memory.
+ *   q        [B, Hq, Nq, D] bf16, contiguous: Nq query tokens per head. Query
+ *            head hq attends with kv head hq / (Hq / Hkv).
+ *   cache    five buffers [B, Hkv, t_cap, X] as for tq_decode_kv; tokens
+ *            [0, T) are read. t_cap must be a multiple of 16.
+ *   left_pad NULL, or B int32 device values: batch row b never attends to
+ *            tokens t < left_pad[b].
+ *   Query token n of a head sits at position T - Nq + n and attends to the
+ *   keys t with left_pad[b] <= t <= T - Nq + n. For those,
+ *     o = H( sum_t softmax_t(scale * q . K[t]) * Vrot[t] ) / sqrt(D) * signs
+ *   with K[t] = bf16 of the decoded key row, Vrot[t] = bf16 of centroid *
+ *   scale (rotated domain), scores and weights in fp32, products of bf16
+ *   operands exact, the weights split into two bf16 parts (exact to about
+ *   2^-18 relative), and the inverse rotation in fp32. A row with no valid
+ *   key is zero; a key row that decodes to NaN (a constant key group, see
+ *   the ops.ts header) makes every row that attends to it NaN.
+ *   out      [B, Hq, Nq, D] of out_dtype, contiguous.
+ *   scale    the softmax scale (1/sqrt(D) for standard attention).
+ *   workspace, workspace_bytes: caller-owned device scratch of at least
+ *            tq_decode_attention_workspace_size(B, Hkv, T, D) bytes (16-byte
+ *            aligned) for the per-chunk partial results; it must not be in
+ *            use by another call still running.
+ * Limits: D in {64, 128, 256} (else TQ_ERR_HEAD_DIM); Hq a multiple of Hkv
+ * and (Hq / Hkv) * Nq <= 16 (else TQ_ERR_INVALID_ARG); t_cap % 16 == 0
+ * (else TQ_ERR_ALIGNMENT). B == 0 is a no-op. Two kernels are enqueued on
+ * `stream`: the split pass over token chunks and the combine pass. */
+tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
+                              const void* k_codes, const void* k_scales, const void* k_zeros,
+                              const void* v_codes, const void* v_scales,
+                              int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
+                              int k_bits, int k_signed, int v_bits,
+                              const int32_t* left_pad, float scale, void* out, tq_dtype out_dtype,
+                              void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Bytes of scratch tq_decode_attention needs for these sizes on the current
+ * device (the token chunking follows the device's SM count, so query it with
+ * the same device current). Negative: -TQ_ERR_HEAD_DIM or -TQ_ERR_INVALID_ARG. */
+int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, int64_t D);
+
 /* Human-readable name of a status code (static string). */
 const char* tq_status_string(int status);
 

@@ -33,7 +33,8 @@ def _declared():
 def test_header_declares_the_abi():
     names = _declared()
     for n in ("tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated", "tq_unrotate",
-              "tq_lloyd_max_index", "tq_status_string"):
+              "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
+              "tq_status_string"):
         assert n in names
 
 
@@ -140,3 +141,41 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(tq, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         tq.lib()
+
+
+def _attn(L, D=128, B=2, Hq=8, Hkv=2, Nq=1, T=20, t_cap=32, kb=8, ks=1, vb=3, dtype=1, ptrs=None,
+          left_pad=None, ws_bytes=1 << 30):
+    ptrs = ptrs if ptrs is not None else [0] * 8
+    return L.tq_decode_attention(ptrs[0], B, Hq, Nq, *ptrs[1:6], Hkv, T, D, t_cap, kb, ks, vb, left_pad, 0.1,
+                                 ptrs[6], dtype, ptrs[7], ws_bytes, None)
+
+
+def test_attention_argument_checks(L):
+    assert _attn(L, D=512) == HEAD_DIM and _attn(L, D=96) == HEAD_DIM
+    assert _attn(L, vb=6) == BITS and _attn(L, kb=4, ks=1) == BITS
+    assert _attn(L, dtype=5) == DTYPE
+    assert _attn(L, Hq=6, Hkv=4) == INVALID            # Hq not a multiple of Hkv
+    assert _attn(L, Hq=16, Hkv=2, Nq=3) == INVALID      # 24 query rows per kv head
+    assert _attn(L, Nq=0) == INVALID and _attn(L, T=-1) == INVALID
+    assert _attn(L, T=40, t_cap=32) == INVALID
+    assert _attn(L, t_cap=24) == ALIGN
+    assert _attn(L) == INVALID                          # null buffers
+    assert _attn(L, B=0) == OK
+    base = 1 << 20
+    ptrs = [base + 4096 * i for i in range(8)]
+    for i in range(8):
+        bad = list(ptrs)
+        bad[i] += 8
+        assert _attn(L, ptrs=bad) == ALIGN
+    assert _attn(L, ptrs=ptrs, left_pad=base + 2) == ALIGN
+    assert _attn(L, ptrs=ptrs, ws_bytes=16) == INVALID  # workspace too small
+
+
+def test_attention_workspace_size(L):
+    assert L.tq_decode_attention_workspace_size(2, 2, 100, 512) == -HEAD_DIM
+    assert L.tq_decode_attention_workspace_size(-1, 2, 100, 128) == -INVALID
+    assert L.tq_decode_attention_workspace_size(2, 0, 100, 128) == -INVALID
+    rec = 16 * (128 + 2) * 4
+    n = L.tq_decode_attention_workspace_size(2, 2, 100, 128)
+    assert n > 0 and n % (4 * rec) == 0
+    assert L.tq_decode_attention_workspace_size(2, 2, 0, 128) == 4 * rec  # one (empty) chunk per pair

@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated",
-    "tq_unrotate", "tq_lloyd_max_index",
+    "tq_unrotate", "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
     "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
 ]
 
@@ -69,6 +69,11 @@ def lib() -> ctypes.CDLL:
             L.tq_unrotate.argtypes = [P, I, I64, I64, P, P]
             L.tq_lloyd_max_index.restype = I
             L.tq_lloyd_max_index.argtypes = [P, I64, I, P, P]
+            L.tq_decode_attention.restype = I
+            L.tq_decode_attention.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P,
+                                              ctypes.c_float, P, I, P, I64, P]
+            L.tq_decode_attention_workspace_size.restype = I64
+            L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
             L.tq_status_string.restype = ctypes.c_char_p
             L.tq_status_string.argtypes = [I]
             _lib = L
@@ -199,4 +204,51 @@ def tq_lloyd_max_index(u: torch.Tensor, v_bits: int, out=None, stream=None) -> t
     st = lib().tq_lloyd_max_index(u.data_ptr(), u.numel(), int(v_bits), out.data_ptr(),
                                   _stream_handle(stream, u.device))
     _check(st, "tq_lloyd_max_index")
+    return out
+
+
+def tq_decode_attention_workspace_size(B: int, Hkv: int, T: int, D: int) -> int:
+    """Bytes of scratch tq_decode_attention needs (on the current device)."""
+    r = int(lib().tq_decode_attention_workspace_size(int(B), int(Hkv), int(T), int(D)))
+    if r < 0:
+        raise TQError(-r, "tq_decode_attention_workspace_size")
+    return r
+
+
+def tq_decode_attention(q: torch.Tensor, cache: dict, T: int, k_bits: int, k_signed: bool, v_bits: int,
+                        left_pad=None, scale=None, out_dtype=torch.bfloat16, out=None, workspace=None,
+                        stream=None) -> torch.Tensor:
+    """Attention of bf16 queries q [B,Hq,Nq,D] over tokens [0,T) of a packed
+    cache [B,Hkv,t_cap,*] (t_cap a multiple of 16), output unrotated
+    [B,Hq,Nq,D] of out_dtype. left_pad: int32 device tensor [B] or None.
+    workspace: a uint8 device tensor of at least
+    tq_decode_attention_workspace_size bytes (allocated when None)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [B,Hq,Nq,D] bfloat16 tensor")
+    if out_dtype not in _DTYPE:
+        raise ValueError("out_dtype must be float32 or bfloat16")
+    B, Hq, Nq, D = q.shape
+    Bc, Hkv, t_cap, _ = cache["k_codes"].shape
+    if Bc != B:
+        raise ValueError("q and the cache must have the same batch size")
+    dev = q.device
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, Nq, D), dtype=out_dtype, device=dev)
+    if out.dtype != out_dtype or tuple(out.shape) != (B, Hq, Nq, D) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B,Hq,Nq,D] tensor of out_dtype")
+    lp = 0
+    if left_pad is not None:
+        if left_pad.dtype != torch.int32 or tuple(left_pad.shape) != (B,) or not left_pad.is_contiguous():
+            raise ValueError("left_pad must be a contiguous int32 tensor [B]")
+        lp = left_pad.data_ptr()
+    need = tq_decode_attention_workspace_size(B, Hkv, T, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib().tq_decode_attention(q.data_ptr(), B, Hq, Nq, *_cache_ptrs(cache), Hkv, int(T), D, t_cap,
+                                   int(k_bits), int(bool(k_signed)), int(v_bits), lp or None, float(scale),
+                                   out.data_ptr(), _DTYPE[out_dtype], workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
+    _check(st, "tq_decode_attention")
     return out

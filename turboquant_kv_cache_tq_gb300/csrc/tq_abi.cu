@@ -252,6 +252,101 @@ extern "C" tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, u
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
+namespace tq {
+namespace {
+
+// Tokens per split block of the fused attention: about two waves of four
+// resident blocks per SM over all (batch, kv head) pairs, a multiple of 64
+// (four warps times 16-token tiles) and at least 64.
+long long attn_chunk(long long bhkv, long long T) {
+  const long long target = 8LL * sm_count();
+  long long per = (T * bhkv + target - 1) / target;
+  per = (per + 63) / 64 * 64;
+  return per < 64 ? 64 : per;
+}
+
+long long attn_n_chunks(long long bhkv, long long T) {
+  if (T <= 0) return 1;
+  const long long c = attn_chunk(bhkv, T);
+  return (T + c - 1) / c;
+}
+
+bool attn_head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256; }
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, int64_t D) {
+  if (B < 0 || Hkv < 1 || T < 0 || T > 0x7fffffffLL || B > 0x7fffffffLL || Hkv > 0x7fffffffLL)
+    return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
+  if (!attn_head_dim_ok(D)) return -static_cast<int64_t>(TQ_ERR_HEAD_DIM);
+  const long long bhkv = B * Hkv;
+  if (bhkv > 0x7fffffffLL) return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
+  return static_cast<int64_t>(bhkv * attn_n_chunks(bhkv, T) * kAttnRecordFloats(D) * 4);
+}
+
+extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
+                                         const void* k_codes, const void* k_scales, const void* k_zeros,
+                                         const void* v_codes, const void* v_scales,
+                                         int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
+                                         int k_bits, int k_signed, int v_bits,
+                                         const int32_t* left_pad, float scale, void* out, tq_dtype out_dtype,
+                                         void* workspace, int64_t workspace_bytes, void* stream) {
+  const long long lim = 0x7fffffffLL;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 1 || T < 0 || t_cap < 0) return TQ_ERR_INVALID_ARG;
+  if (!attn_head_dim_ok(D)) return TQ_ERR_HEAD_DIM;
+  if (key_mode(k_bits, k_signed) < 0 || !value_bits_ok(v_bits)) return TQ_ERR_BITS;
+  if (out_dtype != TQ_F32 && out_dtype != TQ_BF16) return TQ_ERR_DTYPE;
+  if (Hq % Hkv != 0 || (Hq / Hkv) * Nq > kAttnMaxRows) return TQ_ERR_INVALID_ARG;
+  if (T > t_cap || t_cap > lim || B > lim || Hq > lim) return TQ_ERR_INVALID_ARG;
+  if (t_cap % 16 != 0) return TQ_ERR_ALIGNMENT;
+  if (B > 0 && (Hq > lim / B || Hq * B > lim / Nq || Hkv * B > lim)) return TQ_ERR_INVALID_ARG;
+  if (B == 0) return TQ_OK;
+  const long long bhkv = B * Hkv;
+  if (t_cap > (1LL << 62) / (bhkv * 512)) return TQ_ERR_INVALID_ARG;
+  const long long n_chunks = attn_n_chunks(bhkv, T);
+  if (bhkv * n_chunks > lim) return TQ_ERR_INVALID_ARG;
+  const long long need = bhkv * n_chunks * kAttnRecordFloats(D) * 4;
+  const void* ptrs[] = {q, k_codes, k_scales, k_zeros, v_codes, v_scales, out, workspace};
+  for (const void* p : ptrs) {
+    if (!p) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TQ_ERR_ALIGNMENT;
+  }
+  if ((reinterpret_cast<uintptr_t>(left_pad) & 3u) != 0) return TQ_ERR_ALIGNMENT;
+  if (workspace_bytes < need) return TQ_ERR_INVALID_ARG;
+  AttnParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_codes = static_cast<const uint8_t*>(k_codes);
+  p.k_scales = static_cast<const uint16_t*>(k_scales);
+  p.k_zeros = static_cast<const uint16_t*>(k_zeros);
+  p.v_codes = static_cast<const uint8_t*>(v_codes);
+  p.v_scales = static_cast<const uint16_t*>(v_scales);
+  p.left_pad = left_pad;
+  p.ws = static_cast<float*>(workspace);
+  p.out = out;
+  p.B = static_cast<int>(B);
+  p.Hq = static_cast<int>(Hq);
+  p.Hkv = static_cast<int>(Hkv);
+  p.G = static_cast<int>(Hq / Hkv);
+  p.Nq = static_cast<int>(Nq);
+  p.T = static_cast<int>(T);
+  p.t_cap = t_cap;
+  p.chunk = static_cast<int>(attn_chunk(bhkv, T));
+  p.n_chunks = static_cast<int>(n_chunks);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.rot_scale = rotation_scale(D);
+  const int kmode = key_mode(k_bits, k_signed);
+  const bool bf16 = out_dtype == TQ_BF16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (D) {
+    case 64: e = launch_attention<64>(p, v_bits, kmode, bf16, s); break;
+    case 128: e = launch_attention<128>(p, v_bits, kmode, bf16, s); break;
+    default: e = launch_attention<256>(p, v_bits, kmode, bf16, s); break;
+  }
+  return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 extern "C" const char* tq_status_string(int status) {
   switch (status) {
     case TQ_OK: return "TQ_OK";

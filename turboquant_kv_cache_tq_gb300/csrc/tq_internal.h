@@ -60,6 +60,30 @@ struct UnrotateParams {
   float rot_scale;
 };
 
+// Fused decode attention: at most 16 query rows per kv head (Hq/Hkv heads
+// times Nq tokens); one partial record per split block holds m[16], l[16]
+// and O[16][D] as floats.
+constexpr int kAttnMaxRows = 16;
+constexpr long long kAttnRecordFloats(long long D) { return kAttnMaxRows * (D + 2); }
+
+struct AttnParams {
+  const uint16_t* q;    // [B, Hq, Nq, D] bf16 queries
+  const uint8_t* k_codes;
+  const uint16_t* k_scales;
+  const uint16_t* k_zeros;
+  const uint8_t* v_codes;
+  const uint16_t* v_scales;
+  const int* left_pad;  // [B] or null
+  float* ws;            // [B*Hkv*n_chunks] partial records
+  void* out;            // [B, Hq, Nq, D] fp32 or bf16
+  int B, Hq, Hkv, G, Nq, T;
+  long long t_cap;      // multiple of 16
+  int chunk;            // tokens per split block, a multiple of 64
+  int n_chunks;
+  float scale_log2;     // softmax scale * log2(e)
+  float rot_scale;      // fp32(1/sqrt(D))
+};
+
 // Launchers per head_dim (tq_encode_d<D>.cu, tq_decode_d<D>.cu); v_bits in {2,3,4,5,8}.
 template <int D>
 cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaStream_t s);
@@ -67,6 +91,9 @@ template <int D>
 cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s);
 template <int D>
 cudaError_t launch_unrotate(const UnrotateParams& p, bool bf16, cudaStream_t s);
+
+template <int D>
+cudaError_t launch_attention(const AttnParams& p, int v_bits, int kmode, bool out_bf16, cudaStream_t s);
 
 cudaError_t launch_lloyd_max_index(const float* u, long long n, int v_bits, uint8_t* idx, cudaStream_t s);
 
