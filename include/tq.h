@@ -159,6 +159,37 @@ tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
  * the same device current). Negative: -TQ_ERR_HEAD_DIM or -TQ_ERR_INVALID_ARG. */
 int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, int64_t D);
 
+/* tq_decode_attention for callers that cannot allocate device memory: no
+ * counterpart on the pages (an interface addition of this library). Some
+ * callers may not call cudaMalloc: a plugin inside a serving runtime that
+ * reserves the device's memory budget at start-up and owns every allocation
+ * afterwards, or code on a latency-bound path where an allocation (which can
+ * synchronize the device) is not acceptable. Such a caller cannot provide the
+ * workspace tq_decode_attention needs. This call takes the same arguments
+ * minus the workspace and uses a fixed scratch array compiled into the
+ * library instead (TQ_ATTENTION_NOALLOC_SCRATCH_BYTES of device memory, held
+ * on every GPU that loads the library until the process exits). It allocates
+ * nothing.
+ *   - Returns TQ_ERR_INVALID_ARG when the scratch these sizes need,
+ *     tq_decode_attention_workspace_size(B, Hkv, T, D), is larger than
+ *     TQ_ATTENTION_NOALLOC_SCRATCH_BYTES; every other check and result is
+ *     that of tq_decode_attention.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture. TQ_ERR_CUDA if the lookup fails.
+ *   - All calls share the one array: two calls whose work can overlap on the
+ *     GPU (streams with no ordering between them) race. Order them on one
+ *     stream or with events. Nothing in the array needs clearing between
+ *     calls: each call writes every scratch record it reads. */
+#define TQ_ATTENTION_NOALLOC_SCRATCH_BYTES (16LL << 20)
+tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64_t Hq, int64_t Nq,
+                                      const void* k_codes, const void* k_scales, const void* k_zeros,
+                                      const void* v_codes, const void* v_scales,
+                                      int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
+                                      int k_bits, int k_signed, int v_bits,
+                                      const int32_t* left_pad, float scale, void* out, tq_dtype out_dtype,
+                                      void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* tq_status_string(int status);
 

@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
             L.tq_decode_attention.restype = I
             L.tq_decode_attention.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P,
                                               ctypes.c_float, P, I, P, I64, P]
+            L.tq_decode_attention_noalloc.restype = I
+            L.tq_decode_attention_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I,
+                                                      I, P, ctypes.c_float, P, I, P]
             L.tq_decode_attention_workspace_size.restype = I64
             L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
             L.tq_status_string.restype = ctypes.c_char_p
