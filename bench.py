@@ -416,11 +416,32 @@ def run_other_workloads(tq, dev, stream, peak):
                 dec_all = _time_launches(lambda: tq.tq_decode_kv(cache, t_cap, w.k_bits, w.k_signed, vb,
                                                                  stream=stream), stream, 3)
                 r["decode_full_cache_us"] = 1e3 * dec_all
+                r["attention"] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak)
             out["%s_v%d" % (name, vb)] = r
             del cache
         del k, v, ko, vo
         torch.cuda.empty_cache()
     return out
+
+
+def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, G=4):
+    """One decode step of fused attention over the whole packed cache (all
+    t_cap tokens valid): Llama-3-8B's 4 query heads per kv head, one query
+    token per sequence. Algorithmic bytes: the packed cache, read once."""
+    g = torch.Generator(device=dev).manual_seed(6)
+    q = torch.randn((w.B, w.H * G, 1, w.D), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws_bytes = tq.tq_decode_attention_workspace_size(w.B, w.H, t_cap, w.D)
+    work = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ms = _time_launches(lambda: tq.tq_decode_attention(q, cache, t_cap, w.k_bits, w.k_signed, vb, out=out,
+                                                       workspace=work, stream=stream), stream, 10)
+    rows = w.B * w.H * t_cap
+    per_row = w.D * w.k_bits // 8 + w.D * vb // 8 + 3 * (w.D // 32) * 2
+    nbytes = rows * per_row
+    return {"query_heads": w.H * G, "query_tokens": 1, "kv_tokens": t_cap, "us": 1e3 * ms,
+            "bytes_per_launch": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9,
+            "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "kv_tokens_per_s": w.B * t_cap / (ms * 1e-3),
+            "workspace_bytes": ws_bytes, "launches": 2}
 
 
 def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
