@@ -67,14 +67,14 @@ struct AttnLayout {
   static constexpr int VS = VC + kAttnTile * PDV;     // V scales
   static constexpr int END = VS + kAttnTile * NG * 2;
   static constexpr int STAGE = attn_round_up(END + 16, 128);  // + room for word over-reads
-  static constexpr int CENT = attn_round_up(CentroidTable<VB>::kWords * 4, 128);
-  static constexpr int QROW = D + 8;  // bf16 per staged query row (16-byte pad: ldmatrix rows on distinct banks)
-  static constexpr int QBYTES = attn_round_up(kAttnRows * QROW * 2, 128);
+  // value lookup table (see ValueTable): pairs of centroids for widths up to
+  // 4 bits, once per half-warp lane; single centroids once per lane above
+  static constexpr int CENT = VB <= 4 ? (16 * 8) << (2 * VB) : (32 * 4) << VB;
   static constexpr int RING = kAttnWarps * STAGES * STAGE;
   static constexpr int REC = kAttnRows * (D + 2);  // floats of a partial record: m[16], l[16], O[16][D]
   static_assert(REC == kAttnRecordFloats(D), "record layout shared with the host");
   static constexpr int MERGE = kAttnWarps * REC * 4;
-  static constexpr int SMEM = CENT + QBYTES + (RING > MERGE ? RING : MERGE);
+  static constexpr int SMEM = CENT + (RING > MERGE ? RING : MERGE);
   // per-lane element ranges
   static constexpr int EK = D / 4;  // keys: token g, elements [c EK, (c+1) EK)
   static constexpr int EV = D / 8;  // values: elements [g EV, (g+1) EV) of four tokens
@@ -126,12 +126,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&a)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-               : "r"(addr));
-}
-
 // Copy `bytes` (a multiple of 16, compile-time) from global to shared memory
 // with the warp's 16-byte asynchronous copies.
 template <int BYTES>
@@ -142,17 +136,72 @@ __device__ __forceinline__ void copy_region(uint32_t dst, const void* src, int l
   for (int i = lane; i < BYTES / 16; i += 32) cp_async16(dst + 16 * i, s + 16 * i);
 }
 
+// Centroid lookups of the value decode, free of shared-memory bank
+// conflicts. Widths up to 4 bits use a pair table: entry j =
+// (centroid[j & m], centroid[j >> VB]), so the 2 VB-bit field of two
+// consecutive codes (the packing is a little-endian bitstream) fetches both
+// centroids with one 64-bit load; the table is kept once per half-warp lane
+// (entry j for lane L at float2 16 j + L % 16), so the 16 lanes of a
+// half-warp always read 16 distinct bank pairs. Wider codes use the single
+// table kept once per lane (entry j for lane L at word 32 j + L).
+template <int VB>
+struct ValueTable {
+  static constexpr bool PAIRS = VB <= 4;
+};
+
+template <int VB>
+__device__ __forceinline__ void fill_value_table(uint8_t* s) {
+  constexpr int m = (1 << VB) - 1;
+  if constexpr (ValueTable<VB>::PAIRS) {
+    float2* t = reinterpret_cast<float2*>(s);
+    for (int i = threadIdx.x; i < (16 << (2 * VB)); i += blockDim.x) {
+      const int j = i >> 4;
+      t[i] = make_float2(centroid_table<VB>()[j & m], centroid_table<VB>()[j >> VB]);
+    }
+  } else {
+    float* t = reinterpret_cast<float*>(s);
+    for (int i = threadIdx.x; i < (32 << VB); i += blockDim.x) t[i] = centroid_table<VB>()[i >> 5];
+  }
+}
+
+// (field << SH) for the W-bit field at bit `bit` (compile-time) of a
+// little-endian bitstream held in words.
+template <int W, int SH, int NW>
+__device__ __forceinline__ uint32_t field_shl(const uint32_t (&w)[NW], int bit) {
+  const int word = bit >> 5, off = bit & 31;
+  constexpr uint32_t kMask = ((1u << W) - 1u) << SH;
+  if (off + W > 32) return (__funnelshift_r(w[word], w[word + 1], off) << SH) & kMask;
+  if (off >= SH) return (w[word] >> (off - SH)) & kMask;
+  return (w[word] << (SH - off)) & kMask;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  // ex2.approx: relative error below 2^-22; results below 2^-126 flush to
+  // zero, which only drops weights under 2^-126 of the row's largest one
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Transpose of an 8x8 bf16 matrix held as one register per lane (row
+// lane / 4, columns 2 (lane % 4) and 2 (lane % 4) + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 template <int D, int VB, int KMODE, int NT>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) {
   using M = KeySpec<KMODE>;
   constexpr int KB = M::B;
   using L = AttnLayout<D, KB, VB>;
+  using VT = ValueTable<VB>;
   constexpr int S = L::STAGES;
   const float kNegInf = -__int_as_float(0x7f800000);
   extern __shared__ __align__(128) uint8_t smem[];
-  float* s_cent = reinterpret_cast<float*>(smem);
-  uint16_t* s_q = reinterpret_cast<uint16_t*>(smem + L::CENT);
-  uint8_t* s_work = smem + L::CENT + L::QBYTES;
+  uint8_t* s_vtab = smem;
+  uint8_t* s_work = smem + L::CENT;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -161,21 +210,28 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
   const int Rq = p.G * p.Nq;
 
-  fill_centroids<VB>(s_cent);
+  fill_value_table<VB>(s_vtab);
   pdl_launch_dependents();
   pdl_wait();
 
-  // The group's query rows (heads h G .. h G + G - 1, Nq tokens each: Rq
-  // contiguous rows of q) in bf16, head_dim permuted: MMA k index kk of
-  // k-step j holds element (kk % 8 / 2) * D/4 + 4 j + 2 (kk / 8) + kk % 2.
+  // Query operands of the score MMAs, kept in registers: query row 8 n + g
+  // (heads h G .. h G + G - 1, Nq tokens each: Rq contiguous rows of q),
+  // head_dim elements c D/4 + 4 j .. + 3 for k-step j (the contraction's
+  // permuted order: MMA k index kk of k-step j is element
+  // (kk % 8 / 2) D/4 + 4 j + 2 (kk / 8) + kk % 2). Padding rows are zero.
+  uint32_t qf[D / 16][NT][2];
   {
     const uint16_t* qsrc = p.q + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * p.G) * p.Nq * D;
-    for (int i = threadIdx.x; i < kAttnRows * D; i += blockDim.x) {
-      const int r = i / D, d = i - r * D;
-      const int cq = d / L::EK, rem = d - cq * L::EK;
-      const int j = rem >> 2, w4 = rem & 3;
-      const int kk = 2 * cq + (w4 & 1) + 8 * (w4 >> 1);
-      s_q[r * L::QROW + 16 * j + kk] = r < Rq ? qsrc[r * D + d] : static_cast<uint16_t>(0);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int row = 8 * n + g;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        uint2 u = make_uint2(0u, 0u);
+        if (row < Rq) u = *reinterpret_cast<const uint2*>(qsrc + row * D + c * L::EK + 4 * j);
+        qf[j][n][0] = u.x;
+        qf[j][n][1] = u.y;
+      }
     }
   }
   const int t_lo = p.left_pad != nullptr ? max(p.left_pad[b], 0) : 0;
@@ -183,15 +239,20 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
   const int t_end = min(t_beg + p.chunk, p.T);
   t_beg = max(t_beg, t_lo & ~(kAttnTile - 1));
   const int n_tiles = t_end > t_beg ? (t_end - t_beg + kAttnTile - 1) / kAttnTile : 0;
-  // last key of the lane's two score rows (g and g + 8); -1 for padding rows
-  const int hi0 = g < Rq ? p.T - p.Nq + g % p.Nq : -1;
-  const int hi1 = g + 8 < Rq ? p.T - p.Nq + (g + 8) % p.Nq : -1;
+  // last key of the lane's query columns 8 n + 2 c + x; -1 for padding rows
+  int hiq[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int q = 8 * n + 2 * c + x;
+      hiq[n][x] = q < Rq ? p.T - p.Nq + q % p.Nq : -1;
+    }
+  const int t_full = p.T - p.Nq;  // keys up to here are valid for every real row
   __syncthreads();
 
   uint8_t* ring = s_work + warp * S * L::STAGE;
   const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-  const uint32_t q_sh = static_cast<uint32_t>(__cvta_generic_to_shared(s_q)) +
-                        2u * static_cast<uint32_t>((lane & 15) * L::QROW + (lane >> 4) * 8);
   const long long tok0 = static_cast<long long>(bh) * p.t_cap + t_beg;
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
   // Step k of this warp handles tile warp + 4 k in stage k mod S; every step
@@ -216,9 +277,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     for (int n = 0; n < NT; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.0f;
-  float m_run[2] = {kNegInf, kNegInf}, l_run[2] = {0.0f, 0.0f};
-  const float* cent = s_cent + (CentroidTable<VB>::kRep > 1 ? lane : 0);
-  constexpr int kCentStride = CentroidTable<VB>::kRep;
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      m_run[n][x] = kNegInf;
+      l_run[n][x] = 0.0f;
+    }
+  const uint8_t* vtab = s_vtab + (VT::PAIRS ? 8 * (lane & 15) : 4 * lane);
   constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
 
 #pragma unroll
@@ -230,132 +297,170 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     __syncwarp();
     const uint8_t* st = ring + (k % S) * L::STAGE;
     const int t0 = t_beg + (warp + k * kAttnWarps) * kAttnTile;
+    // a tile inside [t_lo, T - Nq] needs no mask (warp-uniform)
+    const bool full = t0 >= t_lo && t0 + kAttnTile - 1 <= t_full;
 
-    // ---- keys: token g of each 8-token half, elements [c EK, (c+1) EK)
+    // ---- keys: tokens g and g + 8, elements [c EK, (c+1) EK)
     uint32_t wk[2][L::NWK];
-    float ks[2][L::KGROUPS], kzb[2][L::KGROUPS];
+    float2 ks2[2][L::KGROUPS], kzb2[2][L::KGROUPS];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int tau = 8 * nt + g;
-      lds_words<L::NWK, L::KALIGN>(st + L::KC + tau * L::PDK, c * (L::EK * KB / 8), wk[nt]);
+    for (int hf = 0; hf < 2; ++hf) {
+      const int tau = g + 8 * hf;
+      lds_words<L::NWK, L::KALIGN>(st + L::KC + tau * L::PDK, c * (L::EK * KB / 8), wk[hf]);
       if constexpr (M::SIGNED) {
 #pragma unroll
-        for (int w = 0; w < L::NWK; ++w) wk[nt][w] ^= 0x80808080u;  // code + 128 in each byte
+        for (int w = 0; w < L::NWK; ++w) wk[hf][w] ^= 0x80808080u;  // code + 128 in each byte
       }
 #pragma unroll
       for (int lg = 0; lg < L::KGROUPS; ++lg) {
         const int grp = (c * L::EK) / kGroup + lg;
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + L::KS);
         const uint16_t* zr = reinterpret_cast<const uint16_t*>(st + L::KZ);
-        ks[nt][lg] = __half2float(__ushort_as_half(sc[tau * L::NG + grp]));
-        kzb[nt][lg] = __fsub_rn(__half2float(__ushort_as_half(zr[tau * L::NG + grp])), kBias);
+        ks2[hf][lg] = f2(__half2float(__ushort_as_half(sc[tau * L::NG + grp])));
+        kzb2[hf][lg] = f2(__fsub_rn(__half2float(__ushort_as_half(zr[tau * L::NG + grp])), kBias));
       }
     }
-    float sacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    // scores S^T = K Q^T: M = the tile's 16 tokens, N = 8 query rows per tile
+    // n, K = 16 head_dim elements per k-step; two accumulator chains
+    float sacc[NT][2][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[n][ch][e] = 0.0f;
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
-      uint32_t a[4];
-      ldmatrix_x4(a, q_sh + 32u * j);
       const int lg = (4 * j) / kGroup;
+      uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float x[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        // four codes as the floats magic + bias + code: one byte permute
+        // each for 8-bit codes
+        uint32_t u[4];
+        if constexpr (KB == 8) {
+          const uint32_t w = wk[hf][j];
+          u[0] = __byte_perm(w, kMagicBits, 0x7640);
+          u[1] = __byte_perm(w, kMagicBits, 0x7641);
+          u[2] = __byte_perm(w, kMagicBits, 0x7642);
+          u[3] = __byte_perm(w, kMagicBits, 0x7643);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // magic + bias + code, then + (zero - magic - bias) = code + zero exactly
-          const float f = __uint_as_float(kMagicBits | code_at<KB>(wk[nt], 4 * j + e));
-          x[e] = __fmul_rn(__fadd_rn(f, kzb[nt][lg]), ks[nt][lg]);
+          for (int e = 0; e < 4; ++e) u[e] = kMagicBits | code_at<KB>(wk[hf], 4 * j + e);
         }
-        mma_bf16_16816(sacc[nt], a, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+        // + (zero - magic - bias) = code + zero exactly, then one rounding
+        // of the product with the scale (decodeKeys), then bf16
+        const float2 x01 = mul2(add2(make_float2(__uint_as_float(u[0]), __uint_as_float(u[1])), kzb2[hf][lg]),
+                                ks2[hf][lg]);
+        const float2 x23 = mul2(add2(make_float2(__uint_as_float(u[2]), __uint_as_float(u[3])), kzb2[hf][lg]),
+                                ks2[hf][lg]);
+        af[hf][0] = pack_bf16x2(x01.x, x01.y);
+        af[hf][1] = pack_bf16x2(x23.x, x23.y);
       }
+      const uint32_t a[4] = {af[0][0], af[1][0], af[0][1], af[1][1]};
+#pragma unroll
+      for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
     }
 
-    // ---- online softmax of rows g (sacc[.][0..1]) and g + 8 (sacc[.][2..3])
-    float xs[2][4];
+    // ---- online softmax per query column 8 n + 2 c + x (tokens g, g + 8
+    // in entries x and 2 + x); the column's values sit in the eight lanes
+    // with the same c
+    float pr[NT][4];
+    float al[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int n = 0; n < NT; ++n) {
+      float xs[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = t0 + 8 * nt + 2 * c + (e & 1);
-        const bool ok = t >= t_lo && t <= (e < 2 ? hi0 : hi1);
-        xs[nt][e] = ok ? __fmul_rn(sacc[nt][e], p.scale_log2) : kNegInf;
-      }
-    float mt0 = fmaxf(fmaxf(xs[0][0], xs[0][1]), fmaxf(xs[1][0], xs[1][1]));
-    float mt1 = fmaxf(fmaxf(xs[0][2], xs[0][3]), fmaxf(xs[1][2], xs[1][3]));
-    mt0 = fmaxf(mt0, __shfl_xor_sync(kFull, mt0, 1));
-    mt0 = fmaxf(mt0, __shfl_xor_sync(kFull, mt0, 2));
-    mt1 = fmaxf(mt1, __shfl_xor_sync(kFull, mt1, 1));
-    mt1 = fmaxf(mt1, __shfl_xor_sync(kFull, mt1, 2));
-    const float mn0 = fmaxf(m_run[0], mt0), mn1 = fmaxf(m_run[1], mt1);
-    const float mu0 = mn0 == kNegInf ? 0.0f : mn0, mu1 = mn1 == kNegInf ? 0.0f : mn1;
-    const float al0 = exp2f(__fsub_rn(m_run[0], mu0)), al1 = exp2f(__fsub_rn(m_run[1], mu1));
-    m_run[0] = mn0;
-    m_run[1] = mn1;
-    float pr[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(__fsub_rn(xs[nt][e], e < 2 ? mu0 : mu1));
-    l_run[0] = __fadd_rn(__fmul_rn(l_run[0], al0),
-                         __fadd_rn(__fadd_rn(pr[0][0], pr[0][1]), __fadd_rn(pr[1][0], pr[1][1])));
-    l_run[1] = __fadd_rn(__fmul_rn(l_run[1], al1),
-                         __fadd_rn(__fadd_rn(pr[0][2], pr[0][3]), __fadd_rn(pr[1][2], pr[1][3])));
-    // rescale O^T: its columns are query rows 2c, 2c + 1 (+ 8 for the second tile)
-    {
-      const float r00 = __shfl_sync(kFull, al0, 8 * c), r01 = __shfl_sync(kFull, al0, 8 * c + 4);
-      const float r10 = __shfl_sync(kFull, al1, 8 * c), r11 = __shfl_sync(kFull, al1, 8 * c + 4);
-      const bool change = r00 != 1.0f || r01 != 1.0f || (NT == 2 && (r10 != 1.0f || r11 != 1.0f));
-      if (__any_sync(kFull, change)) {
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          acc[i][0][0] = __fmul_rn(acc[i][0][0], r00);
-          acc[i][0][1] = __fmul_rn(acc[i][0][1], r01);
-          acc[i][0][2] = __fmul_rn(acc[i][0][2], r00);
-          acc[i][0][3] = __fmul_rn(acc[i][0][3], r01);
-          if constexpr (NT == 2) {
-            acc[i][1][0] = __fmul_rn(acc[i][1][0], r10);
-            acc[i][1][1] = __fmul_rn(acc[i][1][1], r11);
-            acc[i][1][2] = __fmul_rn(acc[i][1][2], r10);
-            acc[i][1][3] = __fmul_rn(acc[i][1][3], r11);
-          }
+        const float sv = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
+        if (full) {
+          xs[e] = __fmul_rn(sv, p.scale_log2);
+        } else {
+          const int t = t0 + g + 8 * (e >> 1);
+          const bool ok = t >= t_lo && t <= hiq[n][e & 1];
+          xs[e] = ok ? __fmul_rn(sv, p.scale_log2) : kNegInf;
         }
       }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        float mt = fmaxf(xs[x], xs[2 + x]);
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+        const float mn = fmaxf(m_run[n][x], mt);
+        const float mu = mn == kNegInf ? 0.0f : mn;
+        al[n][x] = fast_exp2(__fsub_rn(m_run[n][x], mu));
+        m_run[n][x] = mn;
+        pr[n][x] = fast_exp2(__fsub_rn(xs[x], mu));
+        pr[n][2 + x] = fast_exp2(__fsub_rn(xs[2 + x], mu));
+        l_run[n][x] = __fadd_rn(__fmul_rn(l_run[n][x], al[n][x]), __fadd_rn(pr[n][x], pr[n][2 + x]));
+      }
     }
-    // P^T operands (k = token, n = query row) from the score accumulators,
-    // split into bf16 hi + lo
+    // rescale O^T: its columns are this lane's query columns 2 c, 2 c + 1
+    {
+      bool change = false;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) change = change || al[n][0] != 1.0f || al[n][1] != 1.0f;
+      if (__any_sync(kFull, change)) {
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[i][n][0] = __fmul_rn(acc[i][n][0], al[n][0]);
+            acc[i][n][1] = __fmul_rn(acc[i][n][1], al[n][1]);
+            acc[i][n][2] = __fmul_rn(acc[i][n][2], al[n][0]);
+            acc[i][n][3] = __fmul_rn(acc[i][n][3], al[n][1]);
+          }
+      }
+    }
+    // P^T operands (k = token, n = query row): the weights of tokens g and
+    // g + 8 for query columns 2 c, 2 c + 1, split into bf16 hi + lo, then
+    // transposed 8x8 by 8x8
     uint32_t bhi[NT][2], blo[NT][2];
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float p0 = pr[nt][2 * n], p1 = pr[nt][2 * n + 1];
+      for (int hf = 0; hf < 2; ++hf) {
+        const float p0 = pr[n][2 * hf], p1 = pr[n][2 * hf + 1];
         const uint32_t hi = pack_bf16x2(p0, p1);
-        bhi[n][nt] = hi;
-        blo[n][nt] = pack_bf16x2(__fsub_rn(p0, bf16_lo(hi)), __fsub_rn(p1, bf16_hi(hi)));
+        const uint32_t lo = pack_bf16x2(__fsub_rn(p0, bf16_lo(hi)), __fsub_rn(p1, bf16_hi(hi)));
+        bhi[n][hf] = movmatrix_trans(hi);
+        blo[n][hf] = movmatrix_trans(lo);
       }
 
     // ---- values: tokens 2c, 2c + 1, 2c + 8, 2c + 9, elements [g EV, (g+1) EV)
     uint32_t wv[4][L::NWV];
-    float vs[4];
+    float2 vs2[4];
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
       const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
       lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
-      const int t = t0 + tau;
       const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
-      // tokens past T or inside the left pad contribute exactly zero
-      vs[k4] = (t >= t_lo && t < p.T) ? __half2float(__ushort_as_half(sv[tau * L::NG + (g * L::EV) / kGroup])) : 0.0f;
+      float sc = __half2float(__ushort_as_half(sv[tau * L::NG + (g * L::EV) / kGroup]));
+      if (!full) {
+        // tokens past T or inside the left pad contribute exactly zero
+        const int t = t0 + tau;
+        sc = (t >= t_lo && t < p.T) ? sc : 0.0f;
+      }
+      vs2[k4] = f2(sc);
     }
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
-      float v[4][2];
+      // elements 2i, 2i + 1 of each token: RN(centroid * scale), to bf16
+      float2 v[4];
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          v[k4][e] = __fmul_rn(cent[kCentStride * code_at<VB>(wv[k4], 2 * i + e)], vs[k4]);
-      const uint32_t a[4] = {pack_bf16x2(v[0][0], v[1][0]), pack_bf16x2(v[0][1], v[1][1]),
-                             pack_bf16x2(v[2][0], v[3][0]), pack_bf16x2(v[2][1], v[3][1])};
+      for (int k4 = 0; k4 < 4; ++k4) {
+        float2 cc;
+        if constexpr (VT::PAIRS) {
+          cc = *reinterpret_cast<const float2*>(vtab + field_shl<2 * VB, 7>(wv[k4], 2 * i * VB));
+        } else {
+          cc = make_float2(*reinterpret_cast<const float*>(vtab + field_shl<VB, 7>(wv[k4], 2 * i * VB)),
+                           *reinterpret_cast<const float*>(vtab + field_shl<VB, 7>(wv[k4], (2 * i + 1) * VB)));
+        }
+        v[k4] = mul2(cc, vs2[k4]);
+      }
+      const uint32_t a[4] = {pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[0].y, v[1].y),
+                             pack_bf16x2(v[2].x, v[3].x), pack_bf16x2(v[2].y, v[3].y)};
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         mma_bf16_16816(acc[i][n], a, bhi[n][0], bhi[n][1]);
@@ -364,21 +469,27 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     }
   }
   cp_async_wait<0>();
-  // row sums over the four lanes of a row
+  // column sums over the eight lanes of a column
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_run[r] = __fadd_rn(l_run[r], __shfl_xor_sync(kFull, l_run[r], 1));
-    l_run[r] = __fadd_rn(l_run[r], __shfl_xor_sync(kFull, l_run[r], 2));
-  }
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 4));
+      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 8));
+      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 16));
+    }
 
   // ---- merge the four warps in shared memory, one record per block
   __syncthreads();  // every warp is done with its ring
   float* mine = reinterpret_cast<float*>(s_work) + warp * L::REC;
-  if (c == 0) {
-    mine[g] = m_run[0];
-    mine[g + 8] = m_run[1];
-    mine[16 + g] = l_run[0];
-    mine[16 + g + 8] = l_run[1];
+  if (g == 0) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        mine[8 * n + 2 * c + x] = m_run[n][x];
+        mine[16 + 8 * n + 2 * c + x] = l_run[n][x];
+      }
   }
   {
     float* O = mine + 32;
