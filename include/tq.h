@@ -140,12 +140,14 @@ tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx
  *   scale    the softmax scale (1/sqrt(D) for standard attention).
  *   workspace, workspace_bytes: caller-owned device scratch of at least
  *            tq_decode_attention_workspace_size(B, Hkv, T, D) bytes (16-byte
- *            aligned) for the per-chunk partial results; it must not be in
- *            use by another call still running.
+ *            aligned) for the partial results of the split pass (one record
+ *            per split block and kv head it covers); it must not be in use by
+ *            another call still running, and needs no initialisation.
  * Limits: D in {64, 128, 256} (else TQ_ERR_HEAD_DIM); Hq a multiple of Hkv
  * and (Hq / Hkv) * Nq <= 16 (else TQ_ERR_INVALID_ARG); t_cap % 16 == 0
  * (else TQ_ERR_ALIGNMENT). B == 0 is a no-op. Two kernels are enqueued on
- * `stream`: the split pass over token chunks and the combine pass. */
+ * `stream`: the split pass, which cuts the (batch, kv head, 16-token tile)
+ * space evenly over one wave of blocks, and the combine pass. */
 tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
                               const void* k_codes, const void* k_scales, const void* k_zeros,
                               const void* v_codes, const void* v_scales,

@@ -177,5 +177,6 @@ def test_attention_workspace_size(L):
     assert L.tq_decode_attention_workspace_size(2, 0, 100, 128) == -INVALID
     rec = 16 * (128 + 2) * 4
     n = L.tq_decode_attention_workspace_size(2, 2, 100, 128)
-    assert n > 0 and n % (4 * rec) == 0
-    assert L.tq_decode_attention_workspace_size(2, 2, 0, 128) == 4 * rec  # one (empty) chunk per pair
+    # one record per split block (at most 8 per SM) and per (batch, kv head)
+    assert n > 0 and n % rec == 0 and n >= (4 + 8) * rec
+    assert L.tq_decode_attention_workspace_size(2, 3, 100, 128) == n + 2 * rec

@@ -255,21 +255,9 @@ extern "C" tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, u
 namespace tq {
 namespace {
 
-// Tokens per split block of the fused attention: about two waves of four
-// resident blocks per SM over all (batch, kv head) pairs, a multiple of 64
-// (four warps times 16-token tiles) and at least 64.
-long long attn_chunk(long long bhkv, long long T) {
-  const long long target = 8LL * sm_count();
-  long long per = (T * bhkv + target - 1) / target;
-  per = (per + 63) / 64 * 64;
-  return per < 64 ? 64 : per;
-}
-
-long long attn_n_chunks(long long bhkv, long long T) {
-  if (T <= 0) return 1;
-  const long long c = attn_chunk(bhkv, T);
-  return (T + c - 1) / c;
-}
+// Partial records of the fused attention: one per split block and head it
+// touches, at most kAttnGridPerSm blocks per SM plus one per (batch, kv head).
+long long attn_records(long long bhkv) { return static_cast<long long>(kAttnGridPerSm) * sm_count() + bhkv; }
 
 bool attn_head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256; }
 
@@ -282,7 +270,7 @@ extern "C" int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, in
   if (!attn_head_dim_ok(D)) return -static_cast<int64_t>(TQ_ERR_HEAD_DIM);
   const long long bhkv = B * Hkv;
   if (bhkv > 0x7fffffffLL) return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
-  return static_cast<int64_t>(bhkv * attn_n_chunks(bhkv, T) * kAttnRecordFloats(D) * 4);
+  return static_cast<int64_t>(attn_records(bhkv) * kAttnRecordFloats(D) * 4);
 }
 
 extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
@@ -304,9 +292,9 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   if (B == 0) return TQ_OK;
   const long long bhkv = B * Hkv;
   if (t_cap > (1LL << 62) / (bhkv * 512)) return TQ_ERR_INVALID_ARG;
-  const long long n_chunks = attn_n_chunks(bhkv, T);
-  if (bhkv * n_chunks > lim) return TQ_ERR_INVALID_ARG;
-  const long long need = bhkv * n_chunks * kAttnRecordFloats(D) * 4;
+  const long long tiles_per_bh = (T + 15) / 16;
+  if (bhkv * tiles_per_bh > (1LL << 40)) return TQ_ERR_INVALID_ARG;
+  const long long need = attn_records(bhkv) * kAttnRecordFloats(D) * 4;
   const void* ptrs[] = {q, k_codes, k_scales, k_zeros, v_codes, v_scales, out, workspace};
   for (const void* p : ptrs) {
     if (!p) return TQ_ERR_INVALID_ARG;
@@ -331,8 +319,8 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   p.Nq = static_cast<int>(Nq);
   p.T = static_cast<int>(T);
   p.t_cap = t_cap;
-  p.chunk = static_cast<int>(attn_chunk(bhkv, T));
-  p.n_chunks = static_cast<int>(n_chunks);
+  p.tiles_per_bh = static_cast<int>(tiles_per_bh);
+  p.total_tiles = bhkv * tiles_per_bh;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rot_scale = rotation_scale(D);
   const int kmode = key_mode(k_bits, k_signed);

@@ -164,15 +164,18 @@ __device__ __forceinline__ void fill_value_table(uint8_t* s) {
   }
 }
 
-// (field << SH) for the W-bit field at bit `bit` (compile-time) of a
-// little-endian bitstream held in words.
+// (field << SH) | lane_off for the W-bit field at bit `bit` (compile-time)
+// of a little-endian bitstream held in words (one shift and one three-input
+// logic op); lane_off's bits lie below SH or above the field's.
 template <int W, int SH, int NW>
-__device__ __forceinline__ uint32_t field_shl(const uint32_t (&w)[NW], int bit) {
+__device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int bit, uint32_t lane_off) {
   const int word = bit >> 5, off = bit & 31;
   constexpr uint32_t kMask = ((1u << W) - 1u) << SH;
-  if (off + W > 32) return (__funnelshift_r(w[word], w[word + 1], off) << SH) & kMask;
-  if (off >= SH) return (w[word] >> (off - SH)) & kMask;
-  return (w[word] << (SH - off)) & kMask;
+  uint32_t x;
+  if (off + W > 32) x = __funnelshift_r(w[word], w[word + 1], off) << SH;
+  else if (off >= SH) x = w[word] >> (off - SH);
+  else x = w[word] << (SH - off);
+  return (x & kMask) | lane_off;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -205,138 +208,150 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int bh = blockIdx.x / p.n_chunks;
-  const int chunk = blockIdx.x - bh * p.n_chunks;
-  const int b = bh / p.Hkv, h = bh - b * p.Hkv;
   const int Rq = p.G * p.Nq;
 
   fill_value_table<VB>(s_vtab);
   pdl_launch_dependents();
   pdl_wait();
 
-  // Query operands of the score MMAs, kept in registers: query row 8 n + g
-  // (heads h G .. h G + G - 1, Nq tokens each: Rq contiguous rows of q),
-  // head_dim elements c D/4 + 4 j .. + 3 for k-step j (the contraction's
-  // permuted order: MMA k index kk of k-step j is element
-  // (kk % 8 / 2) D/4 + 4 j + 2 (kk / 8) + kk % 2). Padding rows are zero.
-  uint32_t qf[D / 16][NT][2];
-  {
-    const uint16_t* qsrc = p.q + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * p.G) * p.Nq * D;
+  // This block's share of the flattened (batch, kv head, tile) space, cut
+  // into one segment per (batch, kv head) it touches; each segment ends in
+  // one partial record at slot blockIdx.x + bh (unique: the heads of
+  // consecutive blocks never go back).
+  const long long seg_lo = static_cast<long long>(blockIdx.x) * p.total_tiles / gridDim.x;
+  const long long seg_hi = static_cast<long long>(blockIdx.x + 1) * p.total_tiles / gridDim.x;
+  for (long long s0 = seg_lo; s0 < seg_hi;) {
+    const int bh = static_cast<int>(s0 / p.tiles_per_bh);
+    const long long s1 = min(seg_hi, static_cast<long long>(bh + 1) * p.tiles_per_bh);
+    const int tile_lo = static_cast<int>(s0 - static_cast<long long>(bh) * p.tiles_per_bh);
+    const int tile_hi = static_cast<int>(s1 - static_cast<long long>(bh) * p.tiles_per_bh);
+    s0 = s1;
+    const int b = bh / p.Hkv, h = bh - b * p.Hkv;
+    __syncthreads();  // the previous segment's merge area is free again
+
+    // Query operands of the score MMAs, kept in registers: query row 8 n + g
+    // (heads h G .. h G + G - 1, Nq tokens each: Rq contiguous rows of q),
+    // head_dim elements c D/4 + 4 j .. + 3 for k-step j (the contraction's
+    // permuted order: MMA k index kk of k-step j is element
+    // (kk % 8 / 2) D/4 + 4 j + 2 (kk / 8) + kk % 2). Padding rows are zero.
+    uint32_t qf[D / 16][NT][2];
+    {
+      const uint16_t* qsrc = p.q + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * p.G) * p.Nq * D;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int row = 8 * n + g;
+      for (int n = 0; n < NT; ++n) {
+        const int row = 8 * n + g;
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        uint2 u = make_uint2(0u, 0u);
-        if (row < Rq) u = *reinterpret_cast<const uint2*>(qsrc + row * D + c * L::EK + 4 * j);
-        qf[j][n][0] = u.x;
-        qf[j][n][1] = u.y;
+        for (int j = 0; j < D / 16; ++j) {
+          uint2 u = make_uint2(0u, 0u);
+          if (row < Rq) u = *reinterpret_cast<const uint2*>(qsrc + row * D + c * L::EK + 4 * j);
+          qf[j][n][0] = u.x;
+          qf[j][n][1] = u.y;
+        }
       }
     }
-  }
-  const int t_lo = p.left_pad != nullptr ? max(p.left_pad[b], 0) : 0;
-  int t_beg = chunk * p.chunk;
-  const int t_end = min(t_beg + p.chunk, p.T);
-  t_beg = max(t_beg, t_lo & ~(kAttnTile - 1));
-  const int n_tiles = t_end > t_beg ? (t_end - t_beg + kAttnTile - 1) / kAttnTile : 0;
-  // last key of the lane's query columns 8 n + 2 c + x; -1 for padding rows
-  int hiq[NT][2];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int q = 8 * n + 2 * c + x;
-      hiq[n][x] = q < Rq ? p.T - p.Nq + q % p.Nq : -1;
-    }
-  const int t_full = p.T - p.Nq;  // keys up to here are valid for every real row
-  __syncthreads();
-
-  uint8_t* ring = s_work + warp * S * L::STAGE;
-  const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-  const long long tok0 = static_cast<long long>(bh) * p.t_cap + t_beg;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
-  // Step k of this warp handles tile warp + 4 k in stage k mod S; every step
-  // commits one copy group (empty past the end).
-  auto issue = [&](int k) {
-    if (k < my_tiles) {
-      const long long t = tok0 + static_cast<long long>(warp + k * kAttnWarps) * kAttnTile;
-      const uint32_t dst = ring_sh + (k % S) * L::STAGE;
-      copy_region<kAttnTile * L::PDK>(dst + L::KC, p.k_codes + t * L::PDK, lane);
-      copy_region<kAttnTile * L::NG * 2>(dst + L::KS, p.k_scales + t * L::NG, lane);
-      copy_region<kAttnTile * L::NG * 2>(dst + L::KZ, p.k_zeros + t * L::NG, lane);
-      copy_region<kAttnTile * L::PDV>(dst + L::VC, p.v_codes + t * L::PDV, lane);
-      copy_region<kAttnTile * L::NG * 2>(dst + L::VS, p.v_scales + t * L::NG, lane);
-    }
-    cp_async_commit();
-  };
-
-  float acc[D / 16][NT][4];
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i)
+    const int t_lo = p.left_pad != nullptr ? max(p.left_pad[b], 0) : 0;
+    int t_beg = tile_lo * kAttnTile;
+    const int t_end = min(tile_hi * kAttnTile, p.T);
+    t_beg = max(t_beg, t_lo & ~(kAttnTile - 1));
+    const int n_tiles = t_end > t_beg ? (t_end - t_beg + kAttnTile - 1) / kAttnTile : 0;
+    // last key of the lane's query columns 8 n + 2 c + x; -1 for padding rows
+    int hiq[NT][2];
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.0f;
-  float m_run[NT][2], l_run[NT][2];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      m_run[n][x] = kNegInf;
-      l_run[n][x] = 0.0f;
-    }
-  const uint8_t* vtab = s_vtab + (VT::PAIRS ? 8 * (lane & 15) : 4 * lane);
-  constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
-
-#pragma unroll
-  for (int k = 0; k < S - 1; ++k) issue(k);
-  for (int k = 0; k < my_tiles; ++k) {
-    __syncwarp();
-    issue(k + S - 1);
-    cp_async_wait<S - 1>();
-    __syncwarp();
-    const uint8_t* st = ring + (k % S) * L::STAGE;
-    const int t0 = t_beg + (warp + k * kAttnWarps) * kAttnTile;
-    // a tile inside [t_lo, T - Nq] needs no mask (warp-uniform)
-    const bool full = t0 >= t_lo && t0 + kAttnTile - 1 <= t_full;
-
-    // ---- keys: tokens g and g + 8, elements [c EK, (c+1) EK)
-    uint32_t wk[2][L::NWK];
-    float2 ks2[2][L::KGROUPS], kzb2[2][L::KGROUPS];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int tau = g + 8 * hf;
-      lds_words<L::NWK, L::KALIGN>(st + L::KC + tau * L::PDK, c * (L::EK * KB / 8), wk[hf]);
-      if constexpr (M::SIGNED) {
-#pragma unroll
-        for (int w = 0; w < L::NWK; ++w) wk[hf][w] ^= 0x80808080u;  // code + 128 in each byte
+      for (int x = 0; x < 2; ++x) {
+        const int q = 8 * n + 2 * c + x;
+        hiq[n][x] = q < Rq ? p.T - p.Nq + q % p.Nq : -1;
       }
-#pragma unroll
-      for (int lg = 0; lg < L::KGROUPS; ++lg) {
-        const int grp = (c * L::EK) / kGroup + lg;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + L::KS);
-        const uint16_t* zr = reinterpret_cast<const uint16_t*>(st + L::KZ);
-        ks2[hf][lg] = f2(__half2float(__ushort_as_half(sc[tau * L::NG + grp])));
-        kzb2[hf][lg] = f2(__fsub_rn(__half2float(__ushort_as_half(zr[tau * L::NG + grp])), kBias));
+    const int t_full = p.T - p.Nq;  // keys up to here are valid for every real row
+
+    uint8_t* ring = s_work + warp * S * L::STAGE;
+    const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const long long tok0 = static_cast<long long>(bh) * p.t_cap + t_beg;
+    const int my_tiles = n_tiles > warp ? (n_tiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    // Step k of this warp handles tile warp + 4 k in stage k mod S; every step
+    // commits one copy group (empty past the end).
+    auto issue = [&](int k) {
+      if (k < my_tiles) {
+        const long long t = tok0 + static_cast<long long>(warp + k * kAttnWarps) * kAttnTile;
+        const uint32_t dst = ring_sh + (k % S) * L::STAGE;
+        copy_region<kAttnTile * L::PDK>(dst + L::KC, p.k_codes + t * L::PDK, lane);
+        copy_region<kAttnTile * L::NG * 2>(dst + L::KS, p.k_scales + t * L::NG, lane);
+        copy_region<kAttnTile * L::NG * 2>(dst + L::KZ, p.k_zeros + t * L::NG, lane);
+        copy_region<kAttnTile * L::PDV>(dst + L::VC, p.v_codes + t * L::PDV, lane);
+        copy_region<kAttnTile * L::NG * 2>(dst + L::VS, p.v_scales + t * L::NG, lane);
       }
-    }
-    // scores S^T = K Q^T: M = the tile's 16 tokens, N = 8 query rows per tile
-    // n, K = 16 head_dim elements per k-step; two accumulator chains
-    float sacc[NT][2][4];
+      cp_async_commit();
+    };
+
+    float acc[D / 16][NT][4];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][n][e] = 0.0f;
+    float m_run[NT][2], l_run[NT][2];
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
+      for (int x = 0; x < 2; ++x) {
+        m_run[n][x] = kNegInf;
+        l_run[n][x] = 0.0f;
+      }
+    const uint32_t vlane = VT::PAIRS ? 8u * (lane & 15) : 4u * lane;  // the lane's table replica
+    constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
+
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[n][ch][e] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < D / 16; ++j) {
-      const int lg = (4 * j) / kGroup;
-      uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
+    for (int k = 0; k < S - 1; ++k) issue(k);
+    for (int k = 0; k < my_tiles; ++k) {
+      __syncwarp();
+      issue(k + S - 1);
+      cp_async_wait<S - 1>();
+      __syncwarp();
+      const uint8_t* st = ring + (k % S) * L::STAGE;
+      const int t0 = t_beg + (warp + k * kAttnWarps) * kAttnTile;
+      // a tile inside [t_lo, T - Nq] needs no mask (warp-uniform)
+      const bool full = t0 >= t_lo && t0 + kAttnTile - 1 <= t_full;
+
+      // ---- keys: tokens g and g + 8, elements [c EK, (c+1) EK)
+      uint32_t wk[2][L::NWK];
+      float2 ks2[2][L::KGROUPS], kzb2[2][L::KGROUPS];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        // four codes as the floats magic + bias + code: one byte permute
-        // each for 8-bit codes
+        const int tau = g + 8 * hf;
+        lds_words<L::NWK, L::KALIGN>(st + L::KC + tau * L::PDK, c * (L::EK * KB / 8), wk[hf]);
+        if constexpr (M::SIGNED) {
+#pragma unroll
+          for (int w = 0; w < L::NWK; ++w) wk[hf][w] ^= 0x80808080u;  // code + 128 in each byte
+        }
+#pragma unroll
+        for (int lg = 0; lg < L::KGROUPS; ++lg) {
+          const int grp = (c * L::EK) / kGroup + lg;
+          const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + L::KS);
+          const uint16_t* zr = reinterpret_cast<const uint16_t*>(st + L::KZ);
+          ks2[hf][lg] = f2(__half2float(__ushort_as_half(sc[tau * L::NG + grp])));
+          kzb2[hf][lg] = f2(__fsub_rn(__half2float(__ushort_as_half(zr[tau * L::NG + grp])), kBias));
+        }
+      }
+      // scores S^T = K Q^T: M = the tile's 16 tokens, N = 8 query rows per tile
+      // n, K = 16 head_dim elements per k-step; two accumulator chains
+      float sacc[NT][2][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[n][ch][e] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int lg = (4 * j) / kGroup;
+        uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          // four codes as the floats 1.5 * 2^23 + code (+ 128 for signed codes,
+        // whose bytes are offset by flipping their sign bits): one byte
+        // permute each for 8-bit codes
         uint32_t u[4];
         if constexpr (KB == 8) {
           const uint32_t w = wk[hf][j];
@@ -348,191 +363,192 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[e] = kMagicBits | code_at<KB>(wk[hf], 4 * j + e);
         }
-        // + (zero - magic - bias) = code + zero exactly, then one rounding
-        // of the product with the scale (decodeKeys), then bf16
-        const float2 x01 = mul2(add2(make_float2(__uint_as_float(u[0]), __uint_as_float(u[1])), kzb2[hf][lg]),
-                                ks2[hf][lg]);
-        const float2 x23 = mul2(add2(make_float2(__uint_as_float(u[2]), __uint_as_float(u[3])), kzb2[hf][lg]),
-                                ks2[hf][lg]);
+        const float2 f01 = make_float2(__uint_as_float(u[0]), __uint_as_float(u[1]));
+        const float2 f23 = make_float2(__uint_as_float(u[2]), __uint_as_float(u[3]));
+        // + (zero - magic - offset) = code + zero exactly, then one
+        // rounding of the product with the scale (decodeKeys), then bf16
+        const float2 x01 = mul2(add2(f01, kzb2[hf][lg]), ks2[hf][lg]);
+        const float2 x23 = mul2(add2(f23, kzb2[hf][lg]), ks2[hf][lg]);
         af[hf][0] = pack_bf16x2(x01.x, x01.y);
-        af[hf][1] = pack_bf16x2(x23.x, x23.y);
+          af[hf][1] = pack_bf16x2(x23.x, x23.y);
+        }
+        const uint32_t a[4] = {af[0][0], af[1][0], af[0][1], af[1][1]};
+#pragma unroll
+        for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
       }
-      const uint32_t a[4] = {af[0][0], af[1][0], af[0][1], af[1][1]};
-#pragma unroll
-      for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
-    }
 
-    // ---- online softmax per query column 8 n + 2 c + x (tokens g, g + 8
-    // in entries x and 2 + x); the column's values sit in the eight lanes
-    // with the same c
-    float pr[NT][4];
-    float al[NT][2];
+      // ---- online softmax per query column 8 n + 2 c + x (tokens g, g + 8
+      // in entries x and 2 + x); the column's values sit in the eight lanes
+      // with the same c
+      float pr[NT][4];
+      float al[NT][2];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      float xs[4];
+      for (int n = 0; n < NT; ++n) {
+        float xs[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float sv = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
-        if (full) {
-          xs[e] = __fmul_rn(sv, p.scale_log2);
-        } else {
-          const int t = t0 + g + 8 * (e >> 1);
-          const bool ok = t >= t_lo && t <= hiq[n][e & 1];
-          xs[e] = ok ? __fmul_rn(sv, p.scale_log2) : kNegInf;
+        for (int e = 0; e < 4; ++e) {
+          const float sv = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
+          if (full) {
+            xs[e] = __fmul_rn(sv, p.scale_log2);
+          } else {
+            const int t = t0 + g + 8 * (e >> 1);
+            const bool ok = t >= t_lo && t <= hiq[n][e & 1];
+            xs[e] = ok ? __fmul_rn(sv, p.scale_log2) : kNegInf;
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          float mt = fmaxf(xs[x], xs[2 + x]);
+          mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+          mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+          mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+          const float mn = fmaxf(m_run[n][x], mt);
+          const float mu = mn == kNegInf ? 0.0f : mn;
+          al[n][x] = fast_exp2(__fsub_rn(m_run[n][x], mu));
+          m_run[n][x] = mn;
+          pr[n][x] = fast_exp2(__fsub_rn(xs[x], mu));
+          pr[n][2 + x] = fast_exp2(__fsub_rn(xs[2 + x], mu));
+          l_run[n][x] = __fadd_rn(__fmul_rn(l_run[n][x], al[n][x]), __fadd_rn(pr[n][x], pr[n][2 + x]));
         }
       }
+      // rescale O^T: its columns are this lane's query columns 2 c, 2 c + 1
+      {
+        bool change = false;
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        float mt = fmaxf(xs[x], xs[2 + x]);
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
-        const float mn = fmaxf(m_run[n][x], mt);
-        const float mu = mn == kNegInf ? 0.0f : mn;
-        al[n][x] = fast_exp2(__fsub_rn(m_run[n][x], mu));
-        m_run[n][x] = mn;
-        pr[n][x] = fast_exp2(__fsub_rn(xs[x], mu));
-        pr[n][2 + x] = fast_exp2(__fsub_rn(xs[2 + x], mu));
-        l_run[n][x] = __fadd_rn(__fmul_rn(l_run[n][x], al[n][x]), __fadd_rn(pr[n][x], pr[n][2 + x]));
+        for (int n = 0; n < NT; ++n) change = change || al[n][0] != 1.0f || al[n][1] != 1.0f;
+        if (__any_sync(kFull, change)) {
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              acc[i][n][0] = __fmul_rn(acc[i][n][0], al[n][0]);
+              acc[i][n][1] = __fmul_rn(acc[i][n][1], al[n][1]);
+              acc[i][n][2] = __fmul_rn(acc[i][n][2], al[n][0]);
+              acc[i][n][3] = __fmul_rn(acc[i][n][3], al[n][1]);
+            }
+        }
       }
-    }
-    // rescale O^T: its columns are this lane's query columns 2 c, 2 c + 1
-    {
-      bool change = false;
+      // P^T operands (k = token, n = query row): the weights of tokens g and
+      // g + 8 for query columns 2 c, 2 c + 1, split into bf16 hi + lo, then
+      // transposed 8x8 by 8x8
+      uint32_t bhi[NT][2], blo[NT][2];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) change = change || al[n][0] != 1.0f || al[n][1] != 1.0f;
-      if (__any_sync(kFull, change)) {
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i)
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            acc[i][n][0] = __fmul_rn(acc[i][n][0], al[n][0]);
-            acc[i][n][1] = __fmul_rn(acc[i][n][1], al[n][1]);
-            acc[i][n][2] = __fmul_rn(acc[i][n][2], al[n][0]);
-            acc[i][n][3] = __fmul_rn(acc[i][n][3], al[n][1]);
-          }
-      }
-    }
-    // P^T operands (k = token, n = query row): the weights of tokens g and
-    // g + 8 for query columns 2 c, 2 c + 1, split into bf16 hi + lo, then
-    // transposed 8x8 by 8x8
-    uint32_t bhi[NT][2], blo[NT][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float p0 = pr[n][2 * hf], p1 = pr[n][2 * hf + 1];
-        const uint32_t hi = pack_bf16x2(p0, p1);
-        const uint32_t lo = pack_bf16x2(__fsub_rn(p0, bf16_lo(hi)), __fsub_rn(p1, bf16_hi(hi)));
-        bhi[n][hf] = movmatrix_trans(hi);
-        blo[n][hf] = movmatrix_trans(lo);
-      }
+        for (int hf = 0; hf < 2; ++hf) {
+          const float p0 = pr[n][2 * hf], p1 = pr[n][2 * hf + 1];
+          const uint32_t hi = pack_bf16x2(p0, p1);
+          const uint32_t lo = pack_bf16x2(__fsub_rn(p0, bf16_lo(hi)), __fsub_rn(p1, bf16_hi(hi)));
+          bhi[n][hf] = movmatrix_trans(hi);
+          blo[n][hf] = movmatrix_trans(lo);
+        }
 
-    // ---- values: tokens 2c, 2c + 1, 2c + 8, 2c + 9, elements [g EV, (g+1) EV)
-    uint32_t wv[4][L::NWV];
-    float2 vs2[4];
-#pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-      const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-      lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
-      const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
-      float sc = __half2float(__ushort_as_half(sv[tau * L::NG + (g * L::EV) / kGroup]));
-      if (!full) {
-        // tokens past T or inside the left pad contribute exactly zero
-        const int t = t0 + tau;
-        sc = (t >= t_lo && t < p.T) ? sc : 0.0f;
-      }
-      vs2[k4] = f2(sc);
-    }
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      // elements 2i, 2i + 1 of each token: RN(centroid * scale), to bf16
-      float2 v[4];
+      // ---- values: tokens 2c, 2c + 1, 2c + 8, 2c + 9, elements [g EV, (g+1) EV)
+      uint32_t wv[4][L::NWV];
+      float2 vs2[4];
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
-        float2 cc;
-        if constexpr (VT::PAIRS) {
-          cc = *reinterpret_cast<const float2*>(vtab + field_shl<2 * VB, 7>(wv[k4], 2 * i * VB));
-        } else {
-          cc = make_float2(*reinterpret_cast<const float*>(vtab + field_shl<VB, 7>(wv[k4], 2 * i * VB)),
-                           *reinterpret_cast<const float*>(vtab + field_shl<VB, 7>(wv[k4], (2 * i + 1) * VB)));
+        const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
+        lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
+        const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
+        float sc = __half2float(__ushort_as_half(sv[tau * L::NG + (g * L::EV) / kGroup]));
+        if (!full) {
+          // tokens past T or inside the left pad contribute exactly zero
+          const int t = t0 + tau;
+          sc = (t >= t_lo && t < p.T) ? sc : 0.0f;
         }
-        v[k4] = mul2(cc, vs2[k4]);
+        vs2[k4] = f2(sc);
       }
-      const uint32_t a[4] = {pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[0].y, v[1].y),
-                             pack_bf16x2(v[2].x, v[3].x), pack_bf16x2(v[2].y, v[3].y)};
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        mma_bf16_16816(acc[i][n], a, bhi[n][0], bhi[n][1]);
-        mma_bf16_16816(acc[i][n], a, blo[n][0], blo[n][1]);
+      for (int i = 0; i < D / 16; ++i) {
+        // elements 2i, 2i + 1 of each token: RN(centroid * scale), to bf16
+        float2 v[4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          float2 cc;
+          if constexpr (VT::PAIRS) {
+            cc = *reinterpret_cast<const float2*>(s_vtab + field_addr<2 * VB, 7>(wv[k4], 2 * i * VB, vlane));
+          } else {
+            cc = make_float2(*reinterpret_cast<const float*>(s_vtab + field_addr<VB, 7>(wv[k4], 2 * i * VB, vlane)),
+                             *reinterpret_cast<const float*>(s_vtab + field_addr<VB, 7>(wv[k4], (2 * i + 1) * VB, vlane)));
+          }
+          v[k4] = mul2(cc, vs2[k4]);
+        }
+        const uint32_t a[4] = {pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[0].y, v[1].y),
+                               pack_bf16x2(v[2].x, v[3].x), pack_bf16x2(v[2].y, v[3].y)};
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma_bf16_16816(acc[i][n], a, bhi[n][0], bhi[n][1]);
+          mma_bf16_16816(acc[i][n], a, blo[n][0], blo[n][1]);
+        }
       }
     }
-  }
-  cp_async_wait<0>();
-  // column sums over the eight lanes of a column
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 4));
-      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 8));
-      l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 16));
-    }
-
-  // ---- merge the four warps in shared memory, one record per block
-  __syncthreads();  // every warp is done with its ring
-  float* mine = reinterpret_cast<float*>(s_work) + warp * L::REC;
-  if (g == 0) {
+    cp_async_wait<0>();
+    // column sums over the eight lanes of a column
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
-        mine[8 * n + 2 * c + x] = m_run[n][x];
-        mine[16 + 8 * n + 2 * c + x] = l_run[n][x];
+        l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 4));
+        l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 8));
+        l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 16));
       }
-  }
-  {
-    float* O = mine + 32;
+
+    // ---- merge the four warps in shared memory, one record per block
+    __syncthreads();  // every warp is done with its ring
+    float* mine = reinterpret_cast<float*>(s_work) + warp * L::REC;
+    if (g == 0) {
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i)
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const int q0 = 8 * n + 2 * c, d0 = g * L::EV + 2 * i;
-        O[q0 * D + d0] = acc[i][n][0];
-        O[(q0 + 1) * D + d0] = acc[i][n][1];
-        O[q0 * D + d0 + 1] = acc[i][n][2];
-        O[(q0 + 1) * D + d0 + 1] = acc[i][n][3];
+        for (int x = 0; x < 2; ++x) {
+          mine[8 * n + 2 * c + x] = m_run[n][x];
+          mine[16 + 8 * n + 2 * c + x] = l_run[n][x];
+        }
+    }
+    {
+      float* O = mine + 32;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int q0 = 8 * n + 2 * c, d0 = g * L::EV + 2 * i;
+          O[q0 * D + d0] = acc[i][n][0];
+          O[(q0 + 1) * D + d0] = acc[i][n][1];
+          O[q0 * D + d0 + 1] = acc[i][n][2];
+          O[(q0 + 1) * D + d0 + 1] = acc[i][n][3];
+        }
+    }
+    __syncthreads();
+    const float* all = reinterpret_cast<const float*>(s_work);
+    float* rec = p.ws + (static_cast<long long>(blockIdx.x) + bh) * L::REC;
+    for (int i = threadIdx.x; i < Rq * D; i += blockDim.x) {
+      const int r = i / D;
+      float mx = kNegInf;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float mw = all[w * L::REC + r];
+        if (mw != kNegInf) sum = __fadd_rn(sum, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 32 + i]));
       }
-  }
-  __syncthreads();
-  const float* all = reinterpret_cast<const float*>(s_work);
-  float* rec = p.ws + static_cast<long long>(blockIdx.x) * L::REC;
-  for (int i = threadIdx.x; i < Rq * D; i += blockDim.x) {
-    const int r = i / D;
-    float mx = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float mw = all[w * L::REC + r];
-      if (mw != kNegInf) sum = __fadd_rn(sum, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 32 + i]));
+      rec[32 + i] = sum;
     }
-    rec[32 + i] = sum;
-  }
-  for (int r = threadIdx.x; r < Rq; r += blockDim.x) {
-    float mx = kNegInf;
+    for (int r = threadIdx.x; r < Rq; r += blockDim.x) {
+      float mx = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
-    float l = 0.0f;
+      for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
+      float l = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float mw = all[w * L::REC + r];
-      if (mw != kNegInf) l = __fadd_rn(l, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 16 + r]));
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float mw = all[w * L::REC + r];
+        if (mw != kNegInf) l = __fadd_rn(l, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 16 + r]));
+      }
+      rec[r] = mx;
+      rec[16 + r] = l;
     }
-    rec[r] = mx;
-    rec[16 + r] = l;
-  }
+  }  // segments
 }
 
 // Merge of the chunk partials of one output row, normalisation, inverse
@@ -567,14 +583,23 @@ __global__ void __launch_bounds__(kThreads) attn_combine_kernel(AttnParams p) {
     const int hq = rem / p.Nq, n = rem - (rem / p.Nq) * p.Nq;
     const int h = hq / p.G;
     const int r = (hq - h * p.G) * p.Nq + n;
-    const float* recs = p.ws + static_cast<long long>(b * p.Hkv + h) * p.n_chunks * REC;
+    // the split blocks that covered this head's tiles wrote records at
+    // slots (block + bh); block of tile x = floor(((x + 1) grid - 1) / total)
+    const int bh = b * p.Hkv + h;
+    int c0 = 0, n_rec = 0;
+    if (p.tiles_per_bh > 0) {
+      const long long x0 = static_cast<long long>(bh) * p.tiles_per_bh, x1 = x0 + p.tiles_per_bh - 1;
+      c0 = static_cast<int>(((x0 + 1) * p.grid - 1) / p.total_tiles);
+      n_rec = static_cast<int>(((x1 + 1) * p.grid - 1) / p.total_tiles) - c0 + 1;
+    }
+    const float* recs = p.ws + (static_cast<long long>(c0) + bh) * REC;
     float mx = kNegInf;
-    for (int s = 0; s < p.n_chunks; ++s) mx = fmaxf(mx, recs[s * REC + r]);
+    for (int s = 0; s < n_rec; ++s) mx = fmaxf(mx, recs[s * REC + r]);
     float x[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = 0.0f;
     float den = 0.0f;
-    for (int s = 0; s < p.n_chunks; ++s) {
+    for (int s = 0; s < n_rec; ++s) {
       const float* rec = recs + s * REC;
       const float ms = rec[r];
       if (ms == kNegInf) continue;
@@ -624,18 +649,31 @@ inline cudaError_t launch_pdl_block(void (*kernel)(Params), int grid, int block,
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Sets p.grid to the split grid it launches.
 template <int D, int VB, int KMODE, int NT>
-cudaError_t launch_attn_split_t(const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
   using L = AttnLayout<D, KeySpec<KMODE>::B, VB>;
   static const cudaError_t attr = cudaFuncSetAttribute(attn_split_kernel<D, VB, KMODE, NT>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (attr != cudaSuccess) return attr;
-  const int grid = p.B * p.Hkv * p.n_chunks;
-  return launch_pdl_block(attn_split_kernel<D, VB, KMODE, NT>, grid, kAttnThreads, p, s, L::SMEM);
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<D, VB, KMODE, NT>, kAttnThreads,
+                                                      L::SMEM) != cudaSuccess || n < 1)
+      n = 1;
+    return n;
+  }();
+  // one wave of resident blocks (at most kAttnGridPerSm per SM, the bound
+  // the workspace is sized for), never more blocks than tiles
+  long long grid = static_cast<long long>(per_sm < kAttnGridPerSm ? per_sm : kAttnGridPerSm) * sm_count();
+  if (grid > p.total_tiles) grid = p.total_tiles;
+  if (grid < 1) grid = 1;
+  p.grid = static_cast<int>(grid);
+  return launch_pdl_block(attn_split_kernel<D, VB, KMODE, NT>, p.grid, kAttnThreads, p, s, L::SMEM);
 }
 
 template <int D, int VB, int NT>
-cudaError_t launch_attn_split_vb(const AttnParams& p, int kmode, cudaStream_t s) {
+cudaError_t launch_attn_split_vb(AttnParams& p, int kmode, cudaStream_t s) {
   switch (kmode) {
     case kK2: return launch_attn_split_t<D, VB, kK2, NT>(p, s);
     case kK4: return launch_attn_split_t<D, VB, kK4, NT>(p, s);
@@ -646,7 +684,7 @@ cudaError_t launch_attn_split_vb(const AttnParams& p, int kmode, cudaStream_t s)
 }
 
 template <int D, int NT>
-cudaError_t launch_attn_split_nt(const AttnParams& p, int v_bits, int kmode, cudaStream_t s) {
+cudaError_t launch_attn_split_nt(AttnParams& p, int v_bits, int kmode, cudaStream_t s) {
   switch (v_bits) {
     case 2: return launch_attn_split_vb<D, 2, NT>(p, kmode, s);
     case 3: return launch_attn_split_vb<D, 3, NT>(p, kmode, s);
@@ -657,7 +695,8 @@ cudaError_t launch_attn_split_nt(const AttnParams& p, int v_bits, int kmode, cud
 }
 
 template <int D>
-cudaError_t launch_attention(const AttnParams& p, int v_bits, int kmode, bool out_bf16, cudaStream_t s) {
+cudaError_t launch_attention(const AttnParams& params, int v_bits, int kmode, bool out_bf16, cudaStream_t s) {
+  AttnParams p = params;
   const int rq = p.G * p.Nq;
   cudaError_t e = rq <= 8 ? launch_attn_split_nt<D, 1>(p, v_bits, kmode, s) : launch_attn_split_nt<D, 2>(p, v_bits, kmode, s);
   if (e != cudaSuccess) return e;

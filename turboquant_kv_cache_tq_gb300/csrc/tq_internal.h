@@ -65,6 +65,9 @@ struct UnrotateParams {
 // and O[16][D] as floats.
 constexpr int kAttnMaxRows = 16;
 constexpr long long kAttnRecordFloats(long long D) { return kAttnMaxRows * (D + 2); }
+// Split blocks per SM at most; the workspace holds (this * SMs + B * Hkv)
+// records.
+constexpr int kAttnGridPerSm = 8;
 
 struct AttnParams {
   const uint16_t* q;    // [B, Hq, Nq, D] bf16 queries
@@ -74,12 +77,13 @@ struct AttnParams {
   const uint8_t* v_codes;
   const uint16_t* v_scales;
   const int* left_pad;  // [B] or null
-  float* ws;            // [B*Hkv*n_chunks] partial records
+  float* ws;            // partial records, one per (split block, head segment)
   void* out;            // [B, Hq, Nq, D] fp32 or bf16
   int B, Hq, Hkv, G, Nq, T;
   long long t_cap;      // multiple of 16
-  int chunk;            // tokens per split block, a multiple of 64
-  int n_chunks;
+  long long total_tiles;  // B * Hkv * tiles_per_bh
+  int tiles_per_bh;     // ceil(T / 16)
+  int grid;             // split blocks (set by the launcher)
   float scale_log2;     // softmax scale * log2(e)
   float rot_scale;      // fp32(1/sqrt(D))
 };
