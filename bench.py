@@ -417,6 +417,7 @@ def run_other_workloads(tq, dev, stream, peak):
                                                                  stream=stream), stream, 3)
                 r["decode_full_cache_us"] = 1e3 * dec_all
                 r["attention"] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak)
+                r["batched_merge"] = time_merge(tq, w, cache, t_cap, dev, stream, peak)
             out["%s_v%d" % (name, vb)] = r
             del cache
         del k, v, ko, vo
@@ -442,6 +443,23 @@ def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, G=4):
             "bytes_per_launch": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9,
             "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "kv_tokens_per_s": w.B * t_cap / (ms * 1e-3),
             "workspace_bytes": ws_bytes, "launches": 2}
+
+
+def time_merge(tq, w, cache, t_cap, dev, stream, peak):
+    """Continuous batching: merge the cache's B rows, each with its own length
+    (t_cap - 64 i tokens), into a fresh left-padded batch (mergeQuantRows).
+    Bytes: every valid source token row read, the whole window written."""
+    B = w.B
+    lens = [t_cap - 64 * (i % 32) for i in range(B)]
+    width = max(lens)
+    rows = [({k: v[i:i + 1] for k, v in cache.items()}, n) for i, n in enumerate(lens)]
+    dst = tq.alloc_cache(B, w.H, width, w.D, w.k_bits, cache["v_codes"].shape[-1] * 8 // w.D, device=dev)
+    srcs = [(c, 0, 0, n) for c, n in rows]
+    ms = _time_launches(lambda: tq.tq_cache_assemble(srcs, dst, width, stream=stream), stream, 10)
+    per_tok = sum(t.shape[-1] * t.element_size() for t in cache.values()) * w.H
+    nbytes = per_tok * (sum(lens) + B * width)
+    return {"rows": B, "width": width, "us": 1e3 * ms, "bytes_per_launch": nbytes,
+            "GBps": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / peak}
 
 
 def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):

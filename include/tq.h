@@ -192,6 +192,44 @@ tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64_t Hq, int6
                                       const int32_t* left_pad, float scale, void* out, tq_dtype out_dtype,
                                       void* stream);
 
+/* One source row of tq_cache_assemble: tokens [t_start, t_start + len) of
+ * batch row b of a packed cache (five buffers [B, H, t_cap, X], as above,
+ * with the destination's H, D and bit widths). Pointers may be NULL when
+ * len == 0 (an all-padding row). */
+typedef struct {
+    const void* k_codes;
+    const void* k_scales;
+    const void* k_zeros;
+    const void* v_codes;
+    const void* v_scales;
+    int64_t B;       /* batch rows of the source cache */
+    int64_t b;       /* the batch row read, 0 <= b < B */
+    int64_t t_cap;   /* token capacity of the source cache */
+    int64_t t_start; /* first token read */
+    int64_t len;     /* tokens read, 0 <= len <= width, t_start + len <= t_cap */
+} tq_row_source;
+
+/* Batched packed-cache row assembly, the byte-preserving primitive behind
+ * the continuous-batching cache operations of page "@mlx-bun/inference
+ * 0.0.0-stage -> 1.0.0", file batched-quant.ts (mergeQuantRows,
+ * extendQuantRows, extractQuantRow, filterQuantRows): destination batch row
+ * r (of n_rows) receives, for every head and each of the five buffers,
+ * width - rows[r].len zero tokens followed by the source's tokens
+ * [t_start, t_start + len), i.e. the row right-justified in a window of
+ * `width` tokens with its left padding zeroed. Tokens [width, t_cap) of the
+ * destination are not touched. Quantization packs along head_dim only, so
+ * this copies whole token rows and never alters a quantization group.
+ *   rows      host array of n_rows descriptors (read during the call).
+ *   destination: five buffers [n_rows, H, t_cap, X], 16-byte aligned; X from
+ *             D, k_bits, v_bits as for tq_encode_kv. Source and destination
+ *             memory must not overlap.
+ * Sizes and descriptors are checked on the host (TQ_ERR_INVALID_ARG,
+ * TQ_ERR_HEAD_DIM, TQ_ERR_BITS, TQ_ERR_ALIGNMENT) before anything is
+ * enqueued; one kernel is enqueued per 48 destination rows. */
+tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H, int64_t D,
+                            int k_bits, int v_bits, void* k_codes, void* k_scales, void* k_zeros,
+                            void* v_codes, void* v_scales, int64_t t_cap, int64_t width, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* tq_status_string(int status);
 

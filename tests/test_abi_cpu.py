@@ -34,7 +34,7 @@ def test_header_declares_the_abi():
     names = _declared()
     for n in ("tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated", "tq_unrotate",
               "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
-              "tq_status_string"):
+              "tq_decode_attention_noalloc", "tq_cache_assemble", "tq_status_string"):
         assert n in names
 
 
@@ -180,3 +180,27 @@ def test_attention_workspace_size(L):
     # one record per split block (at most 8 per SM) and per (batch, kv head)
     assert n > 0 and n % rec == 0 and n >= (4 + 8) * rec
     assert L.tq_decode_attention_workspace_size(2, 3, 100, 128) == n + 2 * rec
+
+
+def test_cache_assemble_checks(L):
+    import turboquant_kv_cache_tq_gb300 as tq
+
+    base = 1 << 20
+    d = [base + 4096 * i for i in range(5)]
+
+    def call(rows, n=1, H=2, D=128, kb=8, vb=3, t_cap=16, width=8, dst=d):
+        arr = (tq.TQRowSource * max(len(rows), 1))(*rows)
+        return L.tq_cache_assemble(ctypes.cast(arr, ctypes.c_void_p), n, H, D, kb, vb, *dst, t_cap, width, None)
+
+    src = [base + 8192 * i for i in range(5)]
+    ok_row = tq.TQRowSource(*src, 1, 0, 16, 0, 8)
+    assert call([ok_row], D=96) == HEAD_DIM
+    assert call([ok_row], kb=3) == BITS and call([ok_row], vb=6) == BITS
+    assert call([ok_row], width=20) == INVALID                                   # window past capacity
+    assert call([tq.TQRowSource(*src, 1, 0, 16, 10, 8)]) == INVALID             # source range past t_cap
+    assert call([tq.TQRowSource(*src, 1, 1, 16, 0, 8)]) == INVALID              # b >= B
+    assert call([tq.TQRowSource(*src, 1, 0, 16, 0, 9)]) == INVALID              # len > width
+    assert call([tq.TQRowSource(None, *src[1:], 1, 0, 16, 0, 8)]) == INVALID    # null source
+    assert call([tq.TQRowSource(src[0] + 4, *src[1:], 1, 0, 16, 0, 8)]) == ALIGN
+    assert call([ok_row], dst=[d[0] + 8] + d[1:]) == ALIGN
+    assert call([ok_row], n=0) == OK and call([ok_row], width=0) == OK

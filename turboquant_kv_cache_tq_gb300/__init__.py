@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated",
     "tq_unrotate", "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
+    "tq_cache_assemble", "merge_rows", "extend_rows", "extract_row", "filter_rows",
     "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
 ]
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
                                                       I, P, ctypes.c_float, P, I, P]
             L.tq_decode_attention_workspace_size.restype = I64
             L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
+            L.tq_cache_assemble.restype = I
+            L.tq_cache_assemble.argtypes = [P, I64, I64, I64, I, I, P, P, P, P, P, I64, I64, P]
             L.tq_status_string.restype = ctypes.c_char_p
             L.tq_status_string.argtypes = [I]
             _lib = L
@@ -255,3 +258,84 @@ def tq_decode_attention(q: torch.Tensor, cache: dict, T: int, k_bits: int, k_sig
                                    workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _check(st, "tq_decode_attention")
     return out
+
+
+# ---- batched packed-cache rows (batched-quant.ts) ---------------------------------
+class TQRowSource(ctypes.Structure):
+    """tq_row_source of include/tq.h."""
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p), ("k_zeros", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p), ("B", ctypes.c_int64),
+                ("b", ctypes.c_int64), ("t_cap", ctypes.c_int64), ("t_start", ctypes.c_int64),
+                ("len", ctypes.c_int64)]
+
+
+def _cache_geometry(cache: dict):
+    B, H, t_cap, xk = cache["k_codes"].shape
+    D = cache["k_scales"].shape[-1] * GROUP
+    return B, H, t_cap, D, xk * 8 // D, cache["v_codes"].shape[-1] * 8 // D
+
+
+def tq_cache_assemble(sources, dst: dict, width: int, stream=None) -> dict:
+    """Assemble destination batch row r from sources[r] = (cache, b, t_start,
+    length) or None (an all-padding row): width - length zero tokens, then the
+    source's tokens [t_start, t_start + length), for every head and buffer."""
+    n, H, t_cap, D, kb, vb = _cache_geometry(dst)
+    if len(sources) != n:
+        raise ValueError("one source per destination batch row")
+    arr = (TQRowSource * max(n, 1))()
+    for r, src in enumerate(sources):
+        if src is None:
+            arr[r] = TQRowSource(None, None, None, None, None, 0, 0, 0, 0, 0)
+            continue
+        cache, b, t0, length = src
+        Bs, Hs, tcs, Ds, kbs, vbs = _cache_geometry(cache)
+        if (Hs, Ds, kbs, vbs) != (H, D, kb, vb):
+            raise ValueError("source and destination caches differ in heads, head_dim or bit widths")
+        arr[r] = TQRowSource(*_cache_ptrs(cache), Bs, int(b), tcs, int(t0), int(length))
+    st = lib().tq_cache_assemble(ctypes.cast(arr, ctypes.c_void_p), n, H, D, kb, vb, *_cache_ptrs(dst), t_cap,
+                                 int(width), _stream_handle(stream, dst["k_codes"].device))
+    _check(st, "tq_cache_assemble")
+    return dst
+
+
+def _alloc_like(cache: dict, B: int, t_cap: int) -> dict:
+    _, H, _, D, kb, vb = _cache_geometry(cache)
+    return alloc_cache(B, H, t_cap, D, kb, vb, device=cache["k_codes"].device)
+
+
+def merge_rows(rows, t_cap=None, stream=None):
+    """mergeQuantRows: rows = [(cache, length)] single-row caches ([1,H,*,X],
+    tokens [0, length) valid) -> (batch cache [N,H,t_cap,X], left pads, width)
+    with every row right-justified in width = max length."""
+    width = max(int(n) for _, n in rows)
+    pads = [width - int(n) for _, n in rows]
+    dst = _alloc_like(rows[0][0], len(rows), width if t_cap is None else t_cap)
+    tq_cache_assemble([(c, 0, 0, n) for c, n in rows], dst, width, stream)
+    return dst, pads, width
+
+
+def extend_rows(batch, S: int, pads, row, t_cap=None, stream=None):
+    """extendQuantRows: append row = (cache, length) to a batch whose window
+    is S tokens wide; the narrower side is padded on the left."""
+    rc, n = row
+    width = max(int(S), int(n))
+    B = batch["k_codes"].shape[0]
+    dst = _alloc_like(batch, B + 1, width if t_cap is None else t_cap)
+    srcs = [(batch, b, 0, S) for b in range(B)] + [(rc, 0, 0, n)]
+    tq_cache_assemble(srcs, dst, width, stream)
+    return dst, [p + (width - S) for p in pads] + [width - int(n)], width
+
+
+def extract_row(batch, S: int, pad: int, i: int, stream=None) -> dict:
+    """extractQuantRow: batch row i past its left pad as a fresh single-row
+    cache [1, H, S - pad, X]."""
+    dst = _alloc_like(batch, 1, int(S) - int(pad))
+    tq_cache_assemble([(batch, i, pad, int(S) - int(pad))], dst, int(S) - int(pad), stream)
+    return dst
+
+
+def filter_rows(batch, S: int, keep, stream=None) -> dict:
+    """filterQuantRows: the batch rows `keep`, in that order, same window."""
+    dst = _alloc_like(batch, len(keep), batch["k_codes"].shape[2])
+    tq_cache_assemble([(batch, int(b), 0, S) for b in keep], dst, S, stream)
+    return dst
