@@ -1,0 +1,88 @@
+"""Pins of the oracle's Lloyd-Max fit (page "mlx-bun 0.0.9 -> 0.0.11", file
+turboquant-tables.ts: the value tables are an iterative Lloyd-Max fit on a
+unit-normal sample, 500 iterations).
+
+Pins used:
+- a worked example by hand (cells, the boundary tie going to the lower
+  cell, the fixed point reached);
+- the empty-cell reading (an empty cell keeps its centroid);
+- the closed form for two levels on N(0,1): centroids +-sqrt(2/pi);
+- convergence to the page's printed 2-, 4- and 5-bit tables within the
+  sampling error of each cell mean (the page fitted a different sample);
+- Lloyd's descent property: the distortion never increases.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import lloyd_fit as lf
+
+
+def test_worked_example():
+    x = np.array([-3.0, -1.0, 0.0, 2.0, 4.0], np.float32)
+    c1 = lf.lloyd_step(x, np.array([-1.0, 1.0], np.float32))
+    # boundary 0: -3, -1 and 0 (not above the boundary) -> cell 0; 2, 4 -> cell 1
+    assert c1[0] == np.float32(-4.0 / 3.0) and c1[1] == np.float32(3.0)
+    c2 = lf.lloyd_step(x, c1)  # boundary 0.8333: same cells, a fixed point
+    assert np.array_equal(c1, c2)
+    c, b = lf.lloyd_max_fit(x, [-1.0, 1.0], 5)
+    assert np.array_equal(c, c1) and b[0] == np.float32(np.float32(c1[0] + c1[1]) * np.float32(0.5))
+
+
+def test_empty_cells_keep_their_centroids():
+    x = np.array([1.0, 2.0, 3.0], np.float32)
+    c = lf.lloyd_step(x, np.array([-10.0, 1.0, 10.0], np.float32))
+    assert np.array_equal(c, np.array([-10.0, 2.0, 10.0], np.float32))
+
+
+def _normal(n, seed):
+    return np.random.default_rng(seed).standard_normal(n).astype(np.float32)
+
+
+def test_two_levels_closed_form():
+    x = _normal(1 << 20, 1)
+    c, b = lf.lloyd_max_fit(x, [-1.0, 1.0], 30)
+    want = math.sqrt(2.0 / math.pi)
+    assert abs(c[0] + want) < 4e-3 and abs(c[1] - want) < 4e-3 and abs(b[0]) < 4e-3
+
+
+# Max (1960), the minimum-mean-squared-error quantizer of a unit-variance
+# Gaussian: the positive levels for 4, 8 and 16 levels.
+MAX_1960 = {4: [0.4528, 1.510], 8: [0.2451, 0.7560, 1.344, 2.152],
+            16: [0.1284, 0.3881, 0.6568, 0.9424, 1.256, 1.618, 2.069, 2.733]}
+
+
+@pytest.mark.parametrize("K,tol", [(4, 2e-3), (8, 5e-3), (16, 3e-2)])
+def test_converges_to_the_textbook_gaussian_quantizer(K, tol):
+    """The fit of a large N(0,1) sample reaches Max's optimum within the
+    sample's error (largest for the sparse outer cells of 16 levels)."""
+    x = _normal(1 << 20, 2)
+    c, _ = lf.lloyd_max_fit(x, np.linspace(-2.0, 2.0, K), 100)
+    assert np.max(np.abs(c[K // 2:] - np.array(MAX_1960[K]))) < tol
+    assert np.max(np.abs(c[: K // 2][::-1] + np.array(MAX_1960[K]))) < tol
+
+
+@pytest.mark.parametrize("bits", [2, 4, 5])
+def test_printed_tables_are_near_fixed_points(oracle_mod, bits):
+    """Started from the page's printed table, the fit on a large N(0,1)
+    sample moves no centroid by much more than the printed table's own
+    departure from symmetry (the page fitted a smaller sample of its own, and
+    the sparse outer cells vary most from sample to sample)."""
+    x = _normal(1 << 20, 2)
+    printed, _ = oracle_mod.lloyd_max(bits)
+    c, _ = lf.lloyd_max_fit(x, printed, 60)
+    asym = np.max(np.abs(printed + printed[::-1]))
+    assert np.max(np.abs(c - printed)) < 1.5 * asym
+
+
+def test_distortion_never_increases():
+    x = _normal(50000, 3)
+    c = np.linspace(-3.0, 3.0, 16).astype(np.float32)
+    d = lf.distortion(x, c)
+    for _ in range(40):
+        c = lf.lloyd_step(x, c)
+        d2 = lf.distortion(x, c)
+        assert d2 <= d * (1 + 1e-12)
+        d = d2
+    assert np.all(np.diff(c) > 0)
