@@ -321,6 +321,8 @@ def run_ours(args):
     e2e_value = tokens_per_step * e2e["steps"] * ws / (e2e_ms / 1e3)
 
     workloads = run_other_workloads(tq, dev, stream, peak) if args.workloads else None
+    if workloads is not None:
+        workloads["lloyd_max_fit"] = time_lloyd(tq, dev, stream, peak)
 
     cpu = None
     if rank == 0 and ws == 1:
@@ -460,6 +462,24 @@ def time_merge(tq, w, cache, t_cap, dev, stream, peak):
     nbytes = per_tok * (sum(lens) + B * width)
     return {"rows": B, "width": width, "us": 1e3 * ms, "bytes_per_launch": nbytes,
             "GBps": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / peak}
+
+
+def time_lloyd(tq, dev, stream, peak, n=1 << 20, iters=500):
+    """Lloyd-Max table fit (turboquant-tables.ts: 500 iterations on a
+    unit-normal sample) of 2^20 samples at 4 and 8 bits; bytes per
+    iteration = the sample, read once."""
+    g = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn(n, generator=g, device=dev)
+    out = {}
+    for bits in (4, 8):
+        K = 1 << bits
+        init = torch.linspace(-3.0, 3.0, K, device=dev)
+        work = torch.empty(tq.lib().tq_lloyd_max_fit_workspace_size(K), dtype=torch.uint8, device=dev)
+        ms = _time_launches(lambda: tq.tq_lloyd_max_fit(x, init, iters, workspace=work, stream=stream), stream, 3)
+        us_it = 1e3 * ms / iters
+        out["bits%d" % bits] = {"samples": n, "iterations": iters, "ms_per_fit": ms, "us_per_iteration": us_it,
+                                "GBps": 4 * n / (us_it * 1e-6) / 1e9, "frac": 4 * n / (us_it * 1e-6) / 1e9 / peak}
+    return out
 
 
 def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):

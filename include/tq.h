@@ -230,6 +230,31 @@ tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H
                             int k_bits, int v_bits, void* k_codes, void* k_scales, void* k_zeros,
                             void* v_codes, void* v_scales, int64_t t_cap, int64_t width, void* stream);
 
+/* Lloyd-Max fit of a scalar quantizer table, the procedure the tables page
+ * (page "mlx-bun 0.0.9 -> 0.0.11", turboquant-tables.ts header) names for
+ * the LLOYD_MAX value tables: `iters` Lloyd iterations on the fp32 sample
+ * x[0..n) starting from the ascending centroids init[0..levels). One
+ * iteration: boundaries are the fp32 midpoints RN(c_k + c_{k+1}) / 2; each
+ * sample joins cell count(boundaries < x) (the codec's searchsorted); each
+ * centroid becomes its cell's mean (sum / count in float64, rounded once to
+ * fp32); a cell with no samples keeps its centroid. Cell sums are exact
+ * integers in units of 2^-32 (samples of magnitude below 2^-9 are rounded to
+ * that unit), so the result does not depend on the order of additions.
+ *   x          n finite fp32 samples with sum |x| < 2^31 (device).
+ *   levels     2, 4, ..., 256; init, centroids: levels fp32 (device);
+ *              boundaries: levels - 1 fp32 (device), the final midpoints.
+ *   workspace  device scratch of tq_lloyd_max_fit_workspace_size(levels)
+ *              bytes (16-byte aligned; the call clears it first).
+ * One kernel is enqueued per iteration; n < 2^31. */
+tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
+                           float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
+                           void* stream);
+
+/* Bytes of scratch tq_lloyd_max_fit needs (16 + 16 * levels), or
+ * -TQ_ERR_INVALID_ARG for a level count that is not a power of two in
+ * [2, 256]. */
+int64_t tq_lloyd_max_fit_workspace_size(int levels);
+
 /* Human-readable name of a status code (static string). */
 const char* tq_status_string(int status);
 

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated",
     "tq_unrotate", "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
-    "tq_cache_assemble", "merge_rows", "extend_rows", "extract_row", "filter_rows",
+    "tq_cache_assemble", "merge_rows", "extend_rows", "extract_row", "filter_rows", "tq_lloyd_max_fit",
     "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
 ]
 
@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
             L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
             L.tq_cache_assemble.restype = I
             L.tq_cache_assemble.argtypes = [P, I64, I64, I64, I, I, P, P, P, P, P, I64, I64, P]
+            L.tq_lloyd_max_fit.restype = I
+            L.tq_lloyd_max_fit.argtypes = [P, I64, I, I, P, P, P, P, I64, P]
+            L.tq_lloyd_max_fit_workspace_size.restype = I64
+            L.tq_lloyd_max_fit_workspace_size.argtypes = [I]
             L.tq_status_string.restype = ctypes.c_char_p
             L.tq_status_string.argtypes = [I]
             _lib = L
@@ -339,3 +343,23 @@ def filter_rows(batch, S: int, keep, stream=None) -> dict:
     dst = _alloc_like(batch, len(keep), batch["k_codes"].shape[2])
     tq_cache_assemble([(batch, int(b), 0, S) for b in keep], dst, S, stream)
     return dst
+
+
+# ---- Lloyd-Max table fit (turboquant-tables.ts) -----------------------------------
+def tq_lloyd_max_fit(x: torch.Tensor, init: torch.Tensor, iters: int, workspace=None, stream=None):
+    """Lloyd-Max fit of len(init) levels to the fp32 samples x (device), from
+    the ascending centroids init -> (centroids, boundaries), fp32 tensors."""
+    if x.dtype != torch.float32 or init.dtype != torch.float32 or not (x.is_contiguous() and init.is_contiguous()):
+        raise ValueError("x and init must be contiguous float32 tensors")
+    K = init.numel()
+    r = int(lib().tq_lloyd_max_fit_workspace_size(K))
+    if r < 0:
+        raise TQError(-r, "tq_lloyd_max_fit_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(r, dtype=torch.uint8, device=x.device)
+    c = torch.empty(K, dtype=torch.float32, device=x.device)
+    b = torch.empty(max(K - 1, 1), dtype=torch.float32, device=x.device)
+    st = lib().tq_lloyd_max_fit(x.data_ptr(), x.numel(), K, int(iters), init.data_ptr(), c.data_ptr(), b.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(), _stream_handle(stream, x.device))
+    _check(st, "tq_lloyd_max_fit")
+    return c, b[: K - 1]
