@@ -292,3 +292,28 @@ def test_lloyd_max_index_at_boundaries(bits):
     got = tq.tq_lloyd_max_index(torch.from_numpy(u).cuda(), bits).cpu().numpy()
     ref = oracle.searchsorted(b, u)
     assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+
+
+@pytest.mark.parametrize("D,vb", [(128, 8), (64, 5)])
+def test_wide_tables_with_non_finite_rows(D, vb):
+    """Launches of >= 65536 rows at 5 and 8 bits use the per-lane replicated
+    cell table; a warp holding a row whose RMS is not finite (an Inf input)
+    takes the masked path over the full table instead. Every finite row must
+    still match the oracle, including the rows that share a warp with the
+    Inf rows; the Inf rows' indices are unspecified but in bounds."""
+    B, H, T = 1, 1, 65544
+    g = torch.Generator().manual_seed(77 + vb)
+    k = torch.randn((B, H, T, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, T, D), generator=g).to(torch.bfloat16)
+    bad = [5, 40000, 65543]
+    for t in bad:
+        v[0, 0, t, 3] = float("inf")
+    gcache = gpu_encode(k, v, 8, True, vb)
+    rpw = 32 // (D // 32)
+    near = sorted({r for t in bad for r in range((t // rpw) * rpw, (t // rpw) * rpw + rpw) if r not in bad and r < T})
+    rows = np.array(sorted(set(near) | set(_sample_rows(T, 300, vb).tolist()) - set(bad)))
+    ko = to_oracle(k).reshape(-1, D)[rows].reshape(1, 1, -1, D)
+    vo = to_oracle(v).reshape(-1, D)[rows].reshape(1, 1, -1, D)
+    ref = oracle.encode_kv(ko, vo, 8, True, vb)
+    got = {key: val.reshape(-1, val.shape[-1])[rows][None, None] for key, val in cache_to_numpy(gcache).items()}
+    compare_encoded(got, ref, D, vb, v_input=vo.reshape(-1, D))

@@ -67,16 +67,88 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 #ifndef TQ_ENCODE_STAGES
 #define TQ_ENCODE_STAGES 4
 #endif
-template <bool F32>
+template <bool F32, int STAGES = (F32 ? 2 : TQ_ENCODE_STAGES), int THREADS = kThreads>
 struct EncodeRing {
   static constexpr int kLaneBytes = F32 ? 128 : 64;  // 32 inputs
   static constexpr int kChunks = kLaneBytes / 16;
-  static constexpr int kStages = F32 ? 2 : TQ_ENCODE_STAGES;  // a power of two
+  static constexpr int kStages = STAGES;  // a power of two
   static constexpr int kStageBytes = 32 * kLaneBytes;
-  static constexpr int kBlockBytes = (kThreads / 32) * kStages * kStageBytes;
+  static constexpr int kBlockBytes = (THREADS / 32) * kStages * kStageBytes;
   static_assert((kStages & (kStages - 1)) == 0, "stages must be a power of two");
   __device__ static int swz(int lane) { return F32 ? (lane & 7) : ((lane >> 1) & 3); }
 };
+
+// Lloyd-Max cell lookups: the index of every value is one random 64-bit
+// shared load into a cell table (CellGrid), and lanes of a half-warp loading
+// different cells of the same bank pair serialize. With the 256- and
+// 1024-cell tables of 5 and 8 bits those conflicts bound the kernel, so those
+// shapes (bf16 inputs) keep the table once per half-warp lane (entry r for
+// lane L at 16 r + L % 16: the 16 lanes of a half-warp never share a bank),
+// restricted to the cells a finite-RMS group can reach: |v| <= sqrt(32), so
+// cells OFF - R .. OFF + R with R = floor(5.6569 S) + 1 (23 and 93 KB), in one
+// 512-thread block per SM beside a 4-stage ring. Narrower tables conflict
+// less and the extra register would spill at three 256-thread blocks per SM,
+// so those shapes and fp32 inputs keep the shared single table (measured on
+// the long-context cache: v8 encode 393 -> 299 us, v3 302 -> 333 us if
+// replicated too).
+#ifndef TQ_ENCODE_REP_THREADS
+#define TQ_ENCODE_REP_THREADS 512
+#endif
+template <int VB>
+struct RepCells {
+  static constexpr int R = static_cast<int>(5.6569f * CellGrid<VB>::S) + 1;
+  static constexpr int kLo = CellGrid<VB>::OFF - R;
+  static constexpr int kCount = 2 * R + 1;
+  static constexpr int kBytes = kCount * 16 * static_cast<int>(sizeof(CellEntry));
+};
+
+// Cells below and above the replicated range hold no boundary, so clamping a
+// cell into the range leaves the count unchanged.
+template <int VB>
+constexpr bool rep_range_holds_all_boundaries() {
+  for (int j = 0; j < (1 << VB) - 1; ++j) {
+    const int c = grid_cell_host<VB>(lm_boundary<VB>(j));
+    if (c <= RepCells<VB>::kLo || c >= RepCells<VB>::kLo + RepCells<VB>::kCount - 1) return false;
+  }
+  return RepCells<VB>::kLo >= 0 && RepCells<VB>::kLo + RepCells<VB>::kCount <= CellGrid<VB>::NC;
+}
+static_assert(rep_range_holds_all_boundaries<2>() && rep_range_holds_all_boundaries<3>() &&
+                  rep_range_holds_all_boundaries<4>() && rep_range_holds_all_boundaries<5>() &&
+                  rep_range_holds_all_boundaries<8>(),
+              "a boundary lies outside the replicated cell range");
+
+// The replicated table costs each block a 23 or 93 KB fill before its first
+// item, which only pays off on launches of many rows; smaller launches (for
+// instance decode-step appends) take the single-table shape.
+constexpr int kRepMinRows = 65536;
+template <int VB, bool F32, bool ALLOW_REP = true>
+struct EncodeShape {
+  static constexpr bool REP = ALLOW_REP && !F32 && VB >= 5;
+  static constexpr bool WIDE = REP;
+  static constexpr int kBlockThreads = WIDE ? TQ_ENCODE_REP_THREADS : kThreads;
+  static constexpr int kMinBlocks = WIDE ? 1 : kEncodeMinBlocks;
+  using Ring = EncodeRing<F32, F32 ? 2 : TQ_ENCODE_STAGES, kBlockThreads>;
+  static constexpr int kRepBytes = REP ? RepCells<VB>::kBytes : 0;
+  static constexpr int kSmem = Ring::kBlockBytes + kRepBytes;
+};
+
+// Lloyd-Max index of the pair y * inv from the lane's replica of the compact
+// cell table (rep_lane = table + 8 (lane % 16) bytes): the same cell and
+// comparison as lm_index2_scaled, with the cell clamped into the range.
+template <int VB>
+__device__ __forceinline__ void lm_index2_rep(float2 y, float inv, const uint8_t* rep_lane, uint32_t& i0,
+                                              uint32_t& i1) {
+  using G = CellGrid<VB>;
+  using RC = RepCells<VB>;
+  const float2 s = fma2(y, f2(__fmul_rn(inv, G::S)), f2(grid_magic<VB>()));
+  const uint32_t r0 = min(__float_as_uint(s.x) - (kMagicBits + RC::kLo), static_cast<uint32_t>(RC::kCount - 1));
+  const uint32_t r1 = min(__float_as_uint(s.y) - (kMagicBits + RC::kLo), static_cast<uint32_t>(RC::kCount - 1));
+  const CellEntry e0 = *reinterpret_cast<const CellEntry*>(rep_lane + 128u * r0);
+  const CellEntry e1 = *reinterpret_cast<const CellEntry*>(rep_lane + 128u * r1);
+  const float2 d = fma2(y, f2(-inv), make_float2(e0.b, e1.b));
+  i0 = static_cast<uint32_t>(e0.base) + (__float_as_uint(d.x) >> 31);
+  i1 = static_cast<uint32_t>(e1.base) + (__float_as_uint(d.y) >> 31);
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -262,9 +334,11 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
 }
 
 // V encode of the group held by this lane (the whole row's lanes rotate together).
-template <int LPR, int VB, bool F32, typename Prefetch>
+// REP: s_cells is the lane's replica of the compact cell table (bytes, see
+// RepCells) and the rare masked path reads the full table from global memory.
+template <int LPR, int VB, bool F32, bool REP, typename Prefetch>
 __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const uint32_t* s_sign,
-                                                  const CellEntry* s_cells, float rot_scale, float neg_zero,
+                                                  const void* s_cells, float rot_scale, float neg_zero,
                                                   bool store, uint8_t* codes, uint16_t* scale_out,
                                                   Prefetch&& prefetch) {
   uint32_t S[16];
@@ -289,11 +363,16 @@ __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const 
   if (__all_sync(kFull, __float_as_uint(rms) < 0x7f800000u)) {
     // every group of the warp has a finite RMS: cells are in range unmasked
     pack_pairs<VB, false>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
-      lm_index2_scaled<VB, false>(Y[q], inv, s_cells, lo, hi);
+      if constexpr (REP) {
+        lm_index2_rep<VB>(Y[q], inv, static_cast<const uint8_t*>(s_cells), lo, hi);
+      } else {
+        lm_index2_scaled<VB, false>(Y[q], inv, static_cast<const CellEntry*>(s_cells), lo, hi);
+      }
     });
   } else {
+    const CellEntry* tab = REP ? cell_table<VB>() : static_cast<const CellEntry*>(s_cells);
     pack_pairs<VB, false>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
-      lm_index2_scaled<VB, true>(Y[q], inv, s_cells, lo, hi);
+      lm_index2_scaled<VB, true>(Y[q], inv, tab, lo, hi);
     });
   }
   if (store) {
@@ -302,19 +381,28 @@ __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const 
   }
 }
 
-template <int D, int VB, int KMODE, bool F32>
-__global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(EncodeParams p) {
+template <int D, int VB, int KMODE, bool F32, bool ALLOW_REP>
+__global__ void __launch_bounds__(EncodeShape<VB, F32, ALLOW_REP>::kBlockThreads,
+                                  EncodeShape<VB, F32, ALLOW_REP>::kMinBlocks)
+    encode_kernel(EncodeParams p) {
   using G = Geo<D>;
   using M = KeySpec<KMODE>;
-  constexpr int NC = CellGrid<VB>::NC;
+  using SH = EncodeShape<VB, F32, ALLOW_REP>;
+  constexpr int NC = SH::REP ? 1 : CellGrid<VB>::NC;
   constexpr int pdk = D * M::B / 8;
   constexpr int pdv = D * VB / 8;
   constexpr int NG = D / kGroup;
   __shared__ CellEntry s_cells[NC];
   __shared__ __align__(16) uint32_t s_sign[D / 2];
+  extern __shared__ __align__(128) uint8_t s_ring[];
   {
     const CellEntry* tab = cell_table<VB>();
-    for (int i = threadIdx.x; i < NC; i += blockDim.x) s_cells[i] = tab[i];
+    if constexpr (SH::REP) {
+      CellEntry* rep = reinterpret_cast<CellEntry*>(s_ring + SH::Ring::kBlockBytes);
+      for (int i = threadIdx.x; i < RepCells<VB>::kCount * 16; i += blockDim.x) rep[i] = tab[RepCells<VB>::kLo + (i >> 4)];
+    } else {
+      for (int i = threadIdx.x; i < NC; i += blockDim.x) s_cells[i] = tab[i];
+    }
     fill_sign_words<D>(s_sign);
   }
   __syncthreads();
@@ -331,8 +419,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(Enco
 
   // item -> row of this lane (clamped to the last row for a partial tile)
   auto item_row = [&](int it) { const int r0 = (it >> 1) * G::RPW + sub; return r0 < p.rows ? r0 : p.rows - 1; };
-  using R = EncodeRing<F32>;
-  extern __shared__ __align__(128) uint8_t s_ring[];
+  using R = typename SH::Ring;
+  const void* cells = SH::REP ? static_cast<const void*>(s_ring + R::kBlockBytes + 8 * (lane & 15))
+                              : static_cast<const void*>(s_cells);
   uint8_t* lane_ring = s_ring + (threadIdx.x >> 5) * (R::kStages * R::kStageBytes) + lane * R::kLaneBytes;
   const uint32_t lane_ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(lane_ring));
   const int swz = R::swz(lane);
@@ -376,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeMinBlocks) encode_kernel(Enco
       encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l,
                                   p.k_scales + orow * NG + l, p.k_zeros + orow * NG + l, no_prefetch);
     } else {
-      encode_value_item<G::LPR, VB, F32>(in, l, s_sign, s_cells, p.rot_scale, p.neg_zero, valid,
+      encode_value_item<G::LPR, VB, F32, SH::REP>(in, l, s_sign, cells, p.rot_scale, p.neg_zero, valid,
                                          p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l,
                                          no_prefetch);
     }
@@ -618,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
 
 // ---------------------------------------------------------------------------
 template <typename K>
-inline int resident_blocks(K kernel, int dyn_smem = 0) {
+inline int resident_blocks(K kernel, int dyn_smem = 0, int threads = kThreads) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, dyn_smem) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   return per_sm * sm_count();
 }
@@ -628,23 +717,24 @@ inline int resident_blocks(K kernel, int dyn_smem = 0) {
 // Opt a kernel into dynamic shared memory above the default limit, with the
 // largest shared-memory carveout; returns its resident blocks on the device.
 template <typename K>
-inline int prepare_dyn_smem(K kernel, int dyn_smem) {
+inline int prepare_dyn_smem(K kernel, int dyn_smem, int threads = kThreads) {
   cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
   cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  return resident_blocks(kernel, dyn_smem);
+  return resident_blocks(kernel, dyn_smem, threads);
 }
 
-inline int grid_for(long long items, int resident) {
-  const long long needed = (items + (kThreads / 32) - 1) / (kThreads / 32);
+inline int grid_for(long long items, int resident, int threads = kThreads) {
+  const long long needed = (items + (threads / 32) - 1) / (threads / 32);
   return static_cast<int>(needed < resident ? needed : resident);
 }
 
 // Launch with programmatic stream serialization (see the file comment).
 template <typename Params>
-inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p, cudaStream_t s, int dyn_smem = 0) {
+inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p, cudaStream_t s, int dyn_smem = 0,
+                              int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -655,13 +745,24 @@ inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p,
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+template <int D, int VB, int KMODE, bool F32, bool ALLOW_REP>
+cudaError_t launch_encode_shape(const EncodeParams& p, cudaStream_t s) {
+  using SH = EncodeShape<VB, F32, ALLOW_REP>;
+  constexpr int smem = SH::kSmem;
+  constexpr int threads = SH::kBlockThreads;
+  static const int resident = prepare_dyn_smem(encode_kernel<D, VB, KMODE, F32, ALLOW_REP>, smem, threads);
+  const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
+  const cudaError_t e = launch_pdl(encode_kernel<D, VB, KMODE, F32, ALLOW_REP>, grid_for(items, resident, threads), p,
+                                   s, smem, threads);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int D, int VB, int KMODE, bool F32>
 cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
-  constexpr int smem = EncodeRing<F32>::kBlockBytes;
-  static const int resident = prepare_dyn_smem(encode_kernel<D, VB, KMODE, F32>, smem);
-  const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
-  const cudaError_t e = launch_pdl(encode_kernel<D, VB, KMODE, F32>, grid_for(items, resident), p, s, smem);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if constexpr (EncodeShape<VB, F32, true>::REP) {
+    if (p.rows >= kRepMinRows) return launch_encode_shape<D, VB, KMODE, F32, true>(p, s);
+  }
+  return launch_encode_shape<D, VB, KMODE, F32, false>(p, s);
 }
 
 template <int D, int VB, int KMODE, bool F32, bool ROT>
