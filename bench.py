@@ -515,6 +515,49 @@ def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
     return {"ms": e0.elapsed_time(e1), "steps": steps, "h2d": h2d, "d2h": d2h}
 
 
+def run_case(name: str, reps: int):
+    """A small fixed case for profiling one kernel with ncu: the codec on one
+    workload (encode then decode, `reps` times) or one fused decode-attention
+    step over the long-context cache shape. Prints the last timing only; it is
+    not a bench line."""
+    import turboquant_kv_cache_tq_gb300 as tq
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv
+
+    dev = torch.device("cuda")
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if name == "attention":
+        B, H, T, D, G, vb = 32, 8, 8256, 128, 4, 3
+        cache = tq.alloc_cache(B, H, T, D, 8, vb, device=dev)
+        g = torch.Generator(device=dev).manual_seed(0)
+        for b0 in range(0, B, 4):  # encode in slices to keep the footprint small
+            k = (0.5 * torch.randn((4, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
+            v = (0.5 * torch.randn((4, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
+            tq.tq_encode_kv(k, v, 8, True, vb, {n: t[b0:b0 + 4] for n, t in cache.items()})
+            del k, v
+        q = torch.randn((B, H * G, 1, D), generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        work = torch.empty(tq.tq_decode_attention_workspace_size(B, H, T, D), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            e[0].record()
+            tq.tq_decode_attention(q, cache, T, 8, True, vb, out=out, workspace=work)
+            e[1].record()
+        torch.cuda.synchronize()
+        print("attention [32,8,8256,128] k8s v3: %.1f us" % (1e3 * e[0].elapsed_time(e[1])))
+        return
+    w = WORKLOADS[name]
+    k, v = make_kv(w, device=dev)
+    vb = w.v_bits[0]
+    cache = tq.alloc_cache(w.B, w.H, w.T, w.D, w.k_bits, vb, device=dev)
+    ko, vo = torch.empty_like(k), torch.empty_like(v)
+    for _ in range(reps):
+        e[0].record()
+        tq.tq_encode_kv(k, v, w.k_bits, w.k_signed, vb, cache)
+        tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo)
+        e[1].record()
+    torch.cuda.synchronize()
+    print("%s v%d encode+decode: %.1f us" % (name, vb, 1e3 * e[0].elapsed_time(e[1])))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -525,7 +568,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the secondary long-context / hd256 / hd512 measurements")
+    ap.add_argument("--case", default=None,
+                    help="profiling aid: run one small case (a workload name or 'attention') --reps times")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.case:
+        run_case(args.case, args.reps)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
