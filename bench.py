@@ -483,31 +483,64 @@ def time_lloyd(tq, dev, stream, peak, n=1 << 20, iters=500):
 
 
 def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
-    """Host buffers in, host buffers out, through the Python API."""
+    """Host buffers in, host buffers out, through the Python API. Every step
+    copies each layer's K, V from pinned host memory, encodes and decodes it,
+    and copies the decoded K, V back; layers are pipelined over three streams
+    (uploads, kernels, downloads) with per-layer events, so one layer's copies
+    overlap other layers' kernels and the two copy directions overlap each
+    other. A device buffer is rewritten only after its previous reader is done
+    (the next step's upload waits for the layer's encode, its decode for the
+    layer's previous download)."""
     host_in = [(L["k"].cpu().pin_memory(), L["v"].cpu().pin_memory()) for L in layers]
     host_out = [(torch.empty_like(a).pin_memory(), torch.empty_like(b).pin_memory()) for a, b in host_in]
     steps = max(1, min(args.steps, args.e2e_steps))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = len(layers)
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_enc = [torch.cuda.Event() for _ in range(n)]
+    ev_dec = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    started = [False]
 
     def step():
-        for L, (hk, hv), (ok, ov) in zip(layers, host_in, host_out):
-            L["k"].copy_(hk, non_blocking=True)
-            L["v"].copy_(hv, non_blocking=True)
+        for i, (L, (hk, hv), (ok, ov)) in enumerate(zip(layers, host_in, host_out)):
+            with torch.cuda.stream(s_in):
+                if started[0]:
+                    s_in.wait_event(ev_enc[i])  # the previous step's encode has read the inputs
+                L["k"].copy_(hk, non_blocking=True)
+                L["v"].copy_(hv, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
             tq.tq_encode_kv(L["k"], L["v"], kb, ks, vb, L["cache"], stream=stream)
+            ev_enc[i].record(stream)
+            if started[0]:
+                stream.wait_event(ev_out[i])  # the previous step's download has read the outputs
             tq.tq_decode_kv(L["cache"], T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=L["ko"], v_out=L["vo"],
                             stream=stream)
-            ok.copy_(L["ko"], non_blocking=True)
-            ov.copy_(L["vo"], non_blocking=True)
+            ev_dec[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_dec[i])
+                ok.copy_(L["ko"], non_blocking=True)
+                ov.copy_(L["vo"], non_blocking=True)
+                ev_out[i].record(s_out)
+        started[0] = True
 
-    with torch.cuda.stream(stream):
-        step()
+    def join():
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    step()
+    join()
     torch.cuda.synchronize(dev)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
+    e0.record(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    for _ in range(steps):
+        step()
+    join()
+    e1.record(stream)
     e1.synchronize()
     barrier()
     h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_in)
