@@ -349,27 +349,27 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          // four codes as the floats 1.5 * 2^23 + code (+ 128 for signed codes,
-        // whose bytes are offset by flipping their sign bits): one byte
-        // permute each for 8-bit codes
-        uint32_t u[4];
-        if constexpr (KB == 8) {
-          const uint32_t w = wk[hf][j];
-          u[0] = __byte_perm(w, kMagicBits, 0x7640);
-          u[1] = __byte_perm(w, kMagicBits, 0x7641);
-          u[2] = __byte_perm(w, kMagicBits, 0x7642);
-          u[3] = __byte_perm(w, kMagicBits, 0x7643);
-        } else {
+          // four codes as the floats 1.5 * 2^23 + code (+ 128 for signed
+          // codes, whose bytes are offset by flipping their sign bits): one
+          // byte permute each for 8-bit codes
+          uint32_t u[4];
+          if constexpr (KB == 8) {
+            const uint32_t w = wk[hf][j];
+            u[0] = __byte_perm(w, kMagicBits, 0x7640);
+            u[1] = __byte_perm(w, kMagicBits, 0x7641);
+            u[2] = __byte_perm(w, kMagicBits, 0x7642);
+            u[3] = __byte_perm(w, kMagicBits, 0x7643);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) u[e] = kMagicBits | code_at<KB>(wk[hf], 4 * j + e);
-        }
-        const float2 f01 = make_float2(__uint_as_float(u[0]), __uint_as_float(u[1]));
-        const float2 f23 = make_float2(__uint_as_float(u[2]), __uint_as_float(u[3]));
-        // + (zero - magic - offset) = code + zero exactly, then one
-        // rounding of the product with the scale (decodeKeys), then bf16
-        const float2 x01 = mul2(add2(f01, kzb2[hf][lg]), ks2[hf][lg]);
-        const float2 x23 = mul2(add2(f23, kzb2[hf][lg]), ks2[hf][lg]);
-        af[hf][0] = pack_bf16x2(x01.x, x01.y);
+            for (int e = 0; e < 4; ++e) u[e] = kMagicBits | code_at<KB>(wk[hf], 4 * j + e);
+          }
+          const float2 f01 = make_float2(__uint_as_float(u[0]), __uint_as_float(u[1]));
+          const float2 f23 = make_float2(__uint_as_float(u[2]), __uint_as_float(u[3]));
+          // + (zero - magic - offset) = code + zero exactly, then one
+          // rounding of the product with the scale (decodeKeys), then bf16
+          const float2 x01 = mul2(add2(f01, kzb2[hf][lg]), ks2[hf][lg]);
+          const float2 x23 = mul2(add2(f23, kzb2[hf][lg]), ks2[hf][lg]);
+          af[hf][0] = pack_bf16x2(x01.x, x01.y);
           af[hf][1] = pack_bf16x2(x23.x, x23.y);
         }
         const uint32_t a[4] = {af[0][0], af[1][0], af[0][1], af[1][1]};
