@@ -232,3 +232,24 @@ def test_host_checks_on_device_tensors():
         tq.tq_decode_attention(torch.zeros((1, 2, 1, 512), dtype=torch.bfloat16, device="cuda"), cache512, 20,
                                8, True, 3)
     assert e.value.status == 2
+
+
+def test_full_size_long_context_step_sampled_rows():
+    """The bench's attention step at full size and in its launch configuration
+    (cache [32, 8, 8256, 128], k8s, v3, 32 query heads, one query token),
+    checked against the oracle on sampled batch rows (all their heads)."""
+    B, H, T, D, G, vb = 32, 8, 8256, 128, 4, 3
+    cache = tq.alloc_cache(B, H, T, D, 8, vb)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    for b0 in range(0, B, 4):
+        k = (0.5 * torch.randn((4, H, T, D), generator=g, device="cuda")).to(torch.bfloat16)
+        v = (0.5 * torch.randn((4, H, T, D), generator=g, device="cuda")).to(torch.bfloat16)
+        tq.tq_encode_kv(k, v, 8, True, vb, {n: t[b0:b0 + 4] for n, t in cache.items()})
+        del k, v
+    q = torch.randn((B, H * G, 1, D), generator=g, device="cuda").to(torch.bfloat16)
+    got = tq.tq_decode_attention(q, cache, T, 8, True, vb, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for b in (0, 13, 31):
+        sub = cache_to_numpy({n: t[b:b + 1] for n, t in cache.items()})
+        want = oracle.decode_attention(_bits(q[b:b + 1]), sub, T, 8, True, vb)
+        compare_attention(got[b:b + 1].cpu().numpy(), want, _vrot_max(sub, T, 8, True, vb), G, "batch row %d" % b)

@@ -80,3 +80,12 @@ def test_host_checks():
         tq.tq_lloyd_max_fit(x, torch.zeros(3, dtype=torch.float32, device="cuda"), 1)  # not a power of two
     with pytest.raises(tq.TQError):
         tq.tq_lloyd_max_fit(x, torch.zeros(512, dtype=torch.float32, device="cuda"), 1)
+
+
+def test_bench_size_fit():
+    """The bench's fit: 2^20 N(0,1) samples, 500 iterations, 16 levels."""
+    x = np.random.default_rng(7).standard_normal(1 << 20).astype(np.float32)
+    init = np.linspace(-3.0, 3.0, 16).astype(np.float32)
+    c, b = _fit(x, init, 500)
+    rc, rb = lf.lloyd_max_fit(x, init, 500)
+    assert np.max(_ulps(c, rc)) <= 4 and np.max(_ulps(b, rb)) <= 4
