@@ -1,7 +1,7 @@
-// Encode kernels for head_dim 64 (one translation unit per head_dim and
-// direction, so the library builds in parallel).
+// Encode kernels for head_dim 64, bf16 inputs (one translation unit per
+// head_dim, direction and input type, so the library builds in parallel).
 #include "tq_kernels.cuh"
 
 namespace tq {
-template cudaError_t launch_encode<64>(const EncodeParams&, int, bool, cudaStream_t);
+template cudaError_t launch_encode_dt<64, false>(const EncodeParams&, int, cudaStream_t);
 }  // namespace tq
