@@ -548,16 +548,54 @@ def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
     return {"ms": e0.elapsed_time(e1), "steps": steps, "h2d": h2d, "d2h": d2h}
 
 
+def copy_floor(dev, reps: int):
+    """Per-launch time of torch's device copy moving the bytes of one
+    Llama-3-8B-shaped layer encode (11.67 MB read + 11.67 MB written), 32
+    distinct buffers in one CUDA graph, the way the bench times the codec:
+    what a plain memory-bound kernel reaches at this launch size."""
+    n = 23330816 // 4  # int16 elements per copy
+    srcs = [torch.zeros(n, dtype=torch.int16, device=dev) for _ in range(32)]
+    dsts = [torch.empty_like(x) for x in srcs]
+    s = torch.cuda.Stream(dev)
+
+    def body():
+        for a, b in zip(srcs, dsts):
+            b.copy_(a)
+
+    with torch.cuda.stream(s):
+        body()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body()
+    for _ in range(10):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            g.replay()
+    e1.record(s)
+    e1.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps / 32
+    print("copy floor (32 x 11.67 MB copies in a CUDA graph): %.2f us per launch, %.0f GB/s" % (us, 23330816 / us / 1e3))
+
+
 def run_case(name: str, reps: int):
     """A small fixed case for profiling one kernel with ncu: the codec on one
-    workload (encode then decode, `reps` times) or one fused decode-attention
-    step over the long-context cache shape. Prints the last timing only; it is
+    workload (encode then decode, `reps` times), one fused decode-attention
+    step over the long-context cache shape, or the plain-copy floor of the
+    Llama-3-8B-shaped layer ('copy_floor'). Prints the median timing; it is
     not a bench line."""
     import turboquant_kv_cache_tq_gb300 as tq
     from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv
 
     dev = torch.device("cuda")
-    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if name == "copy_floor":
+        copy_floor(dev, max(reps, 20))
+        return
+    e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
     if name == "attention":
         B, H, T, D, G, vb = 32, 8, 8256, 128, 4, 3
         cache = tq.alloc_cache(B, H, T, D, 8, vb, device=dev)
@@ -570,25 +608,31 @@ def run_case(name: str, reps: int):
         q = torch.randn((B, H * G, 1, D), generator=g, device=dev).to(torch.bfloat16)
         out = torch.empty_like(q)
         work = torch.empty(tq.tq_decode_attention_workspace_size(B, H, T, D), dtype=torch.uint8, device=dev)
-        for _ in range(reps):
-            e[0].record()
-            tq.tq_decode_attention(q, cache, T, 8, True, vb, out=out, workspace=work)
-            e[1].record()
         torch.cuda.synchronize()
-        print("attention [32,8,8256,128] k8s v3: %.1f us" % (1e3 * e[0].elapsed_time(e[1])))
+        for r in range(reps):
+            e[r][0].record()
+            tq.tq_decode_attention(q, cache, T, 8, True, vb, out=out, workspace=work)
+            e[r][1].record()
+        torch.cuda.synchronize()
+        print("attention [32,8,8256,128] k8s v3: %.1f us" % _median_us(e))
         return
     w = WORKLOADS[name]
     k, v = make_kv(w, device=dev)
     vb = w.v_bits[0]
     cache = tq.alloc_cache(w.B, w.H, w.T, w.D, w.k_bits, vb, device=dev)
     ko, vo = torch.empty_like(k), torch.empty_like(v)
-    for _ in range(reps):
-        e[0].record()
+    torch.cuda.synchronize()
+    for r in range(reps):
+        e[r][0].record()
         tq.tq_encode_kv(k, v, w.k_bits, w.k_signed, vb, cache)
         tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo)
-        e[1].record()
+        e[r][1].record()
     torch.cuda.synchronize()
-    print("%s v%d encode+decode: %.1f us" % (name, vb, 1e3 * e[0].elapsed_time(e[1])))
+    print("%s v%d encode+decode: %.1f us" % (name, vb, _median_us(e)))
+
+
+def _median_us(events) -> float:
+    return 1e3 * sorted(a.elapsed_time(b) for a, b in events)[len(events) // 2]
 
 
 def main(argv=None):
@@ -602,7 +646,7 @@ def main(argv=None):
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the secondary long-context / hd256 / hd512 measurements")
     ap.add_argument("--case", default=None,
-                    help="profiling aid: run one small case (a workload name or 'attention') --reps times")
+                    help="profiling aid: run one small case (a workload name, 'attention' or 'copy_floor') --reps times")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     if args.case:

@@ -97,11 +97,52 @@ def test_workload_full_size_sampled(name):
         # decode at full size, compare the sampled rows with the oracle's decode
         kd, vd = tq.tq_decode_kv(gcache, w.T, w.k_bits, w.k_signed, vb, out_dtype=torch.float32)
         torch.cuda.synchronize()
-        kr, vr = oracle.decode_kv(ref, len(rows), w.k_bits, w.k_signed, vb)
+        # the oracle decodes the same packed bytes (a value index may differ
+        # from the oracle's encode inside the boundary band)
+        kr, vr = oracle.decode_kv(g, len(rows), w.k_bits, w.k_signed, vb)
         compare_decoded(kd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), kr.reshape(-1, D), "K")
         compare_decoded(vd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), vr.reshape(-1, D), "V")
         del gcache, kd, vd
         torch.cuda.empty_cache()
+
+
+# ---- launches long enough for the interleaved work order -------------------------------
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_long_launches_sampled(D, dtype):
+    """Launches of more than 4 items per warp take the interleaved work order
+    (short ones the snake order, which every small test covers). 4 * 9728 *
+    rows-per-warp + 1 rows exceed 4 steps per warp at any occupancy (at most
+    64 warps per SM on 152 SMs); sampled rows are compared with the oracle,
+    and the decode of the whole launch on the same rows."""
+    rpw = 32 // (D // 32)
+    R = 4 * 152 * 64 * rpw + 1
+    H = 4
+    T = (R + H - 1) // H
+    g = torch.Generator(device="cuda").manual_seed(D + (dtype == torch.float32))
+    k = (torch.randn((1, H, T, D), generator=g, device="cuda") * 1.5).to(dtype)
+    v = torch.randn((1, H, T, D), generator=g, device="cuda").to(dtype)
+    rows = _sample_rows(H * T, 300, D, per_bh=T)
+    kr = to_oracle(k.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu()).reshape(1, 1, -1, D)
+    vr = to_oracle(v.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu()).reshape(1, 1, -1, D)
+    for i, vb in enumerate([2, 3, 4, 5, 8]):
+        kb, ks = KEY_MODES[(i + D // 64) % len(KEY_MODES)]
+        cache = tq.alloc_cache(1, H, T, D, kb, vb)
+        tq.tq_encode_kv(k, v, kb, ks, vb, cache)
+        torch.cuda.synchronize()
+        ref = oracle.encode_kv(kr, vr, kb, ks, vb)
+        got = {n: t.reshape(-1, t.shape[-1])[rows][None, None] for n, t in cache_to_numpy(cache).items()}
+        compare_encoded(got, ref, D, vb, v_input=vr.reshape(-1, D))
+        kd, vd = tq.tq_decode_kv(cache, T, kb, ks, vb, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        # the oracle decodes the same packed bytes (a value index may differ
+        # from the oracle's encode inside the boundary band)
+        kref, vref = oracle.decode_kv(got, len(rows), kb, ks, vb)
+        sel = torch.from_numpy(rows).cuda()
+        compare_decoded(kd.reshape(-1, D)[sel].cpu().numpy(), kref.reshape(-1, D), "K")
+        compare_decoded(vd.reshape(-1, D)[sel].cpu().numpy(), vref.reshape(-1, D), "V")
+        del cache, kd, vd
+    torch.cuda.empty_cache()
 
 
 # ---- appends into a preallocated cache ---------------------------------------------
