@@ -1,8 +1,9 @@
-// Decode kernels for head_dim 128 (one translation unit per head_dim and
-// direction, so the library builds in parallel).
+// Decode kernels for head_dim 128, bf16 outputs, and the unrotate kernel (one
+// translation unit per head_dim, direction and type, so the library builds in
+// parallel).
 #include "tq_kernels.cuh"
 
 namespace tq {
-template cudaError_t launch_decode<128>(const DecodeParams&, int, bool, bool, cudaStream_t);
+template cudaError_t launch_decode_dt<128, false, false>(const DecodeParams&, int, cudaStream_t);
 template cudaError_t launch_unrotate<128>(const UnrotateParams&, bool, cudaStream_t);
 }  // namespace tq

@@ -1,0 +1,7 @@
+// Decode kernels for head_dim 256, fp32 outputs (one translation unit per
+// head_dim, direction and type, so the library builds in parallel).
+#include "tq_kernels.cuh"
+
+namespace tq {
+template cudaError_t launch_decode_dt<256, true, false>(const DecodeParams&, int, cudaStream_t);
+}  // namespace tq

@@ -88,16 +88,24 @@ struct AttnParams {
   float rot_scale;      // fp32(1/sqrt(D))
 };
 
-// Launchers per head_dim (tq_encode_d<D>.cu for bf16 inputs, tq_encode_f32_d<D>.cu
-// for fp32 inputs, tq_decode_d<D>.cu); v_bits in {2,3,4,5,8}.
+// Launchers per head_dim, one translation unit per input or output type (and
+// rotated V for decode): tq_encode_d<D>.cu (bf16 inputs), tq_encode_f32_d<D>.cu,
+// tq_decode_d<D>.cu (bf16 outputs), tq_decode_f32_d<D>.cu, tq_decode_rot_d<D>.cu,
+// tq_decode_rot_f32_d<D>.cu; v_bits in {2,3,4,5,8}.
 template <int D, bool F32>
 cudaError_t launch_encode_dt(const EncodeParams& p, int v_bits, cudaStream_t s);
 template <int D>
 inline cudaError_t launch_encode(const EncodeParams& p, int v_bits, bool in_bf16, cudaStream_t s) {
   return in_bf16 ? launch_encode_dt<D, false>(p, v_bits, s) : launch_encode_dt<D, true>(p, v_bits, s);
 }
+template <int D, bool F32, bool ROT>
+cudaError_t launch_decode_dt(const DecodeParams& p, int v_bits, cudaStream_t s);
 template <int D>
-cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s);
+inline cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s) {
+  if (rotated_v)
+    return out_bf16 ? launch_decode_dt<D, false, true>(p, v_bits, s) : launch_decode_dt<D, true, true>(p, v_bits, s);
+  return out_bf16 ? launch_decode_dt<D, false, false>(p, v_bits, s) : launch_decode_dt<D, true, false>(p, v_bits, s);
+}
 template <int D>
 cudaError_t launch_unrotate(const UnrotateParams& p, bool bf16, cudaStream_t s);
 

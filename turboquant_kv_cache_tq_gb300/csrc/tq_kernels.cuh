@@ -631,8 +631,10 @@ __device__ __forceinline__ float centroid_at(const float* cent, const uint32_t (
 }
 
 // V decode of one group. ROT: leave the values in the rotated domain
-// (dequantScaled / decodeValuesRotated: centroid * scale only).
-template <int LPR, int VB, bool F32, bool ROT, int W, typename Prefetch>
+// (dequantScaled / decodeValuesRotated: centroid * scale only). SIGNS_IN_REGS:
+// s_sign is the lane's own 16 sign words (held in registers by the caller)
+// instead of the block's shared table.
+template <int LPR, int VB, bool F32, bool ROT, bool SIGNS_IN_REGS, int W, typename Prefetch>
 __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, const uint32_t* s_sign,
                                                   const float* s_cent, float rot_scale, float neg_zero,
                                                   bool store, void* out, size_t out_off, Prefetch&& prefetch) {
@@ -658,7 +660,12 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
     const float2 c2 = f2(rot_scale);
 #pragma unroll
     for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], c2);
-    load_sign_words(s_sign, l, S);
+    if constexpr (SIGNS_IN_REGS) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) S[j] = s_sign[j];
+    } else {
+      load_sign_words(s_sign, l, S);
+    }
   }
   if (!store) return;
   if constexpr (!F32) {
@@ -682,11 +689,25 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
   }
 }
 
-template <int D, int VB, int KMODE, bool F32, bool ROT>
+// Decode staging, a template argument chosen per launch like the encode's
+// item order:
+//   SHORT (at most kSnakeSteps steps per warp): the packed inputs of the next
+//   two items are in flight while an item computes, so the first steps of a
+//   launch wait less on memory; the sign words come from shared memory.
+//   Long launches: one item ahead, and (bf16 outputs) each lane keeps its 16
+//   sign words in registers for the whole launch, which takes 16 wavefronts
+//   of shared traffic off every V item (the V items are bound by
+//   shared-memory and shuffle traffic).
+// Measured: the [1, 8, 4096, 128] layer decodes in 7.11 instead of 7.37 us
+// with two items ahead (7.60 us with the register signs); the
+// [32, 8, 8192, 128] cache in 289.8 instead of 303.3 us with the register
+// signs (308.2 us with two items ahead). Both at once spill.
+template <int D, int VB, int KMODE, bool F32, bool ROT, bool SHORT>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(DecodeParams p) {
   using G = Geo<D>;
   using M = KeySpec<KMODE>;
   constexpr int W = M::B > VB ? M::B : VB;
+  constexpr int kAhead = SHORT ? 2 : 1;
   __shared__ float s_cent[CentroidTable<VB>::kWords];
   __shared__ __align__(16) uint32_t s_sign[D / 2];
   fill_centroids<VB>(s_cent);
@@ -709,9 +730,20 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
     const int bh = fast_div(r, p.tdiv);
     return static_cast<long long>(bh) * p.t_cap + (r - bh * p.T);
   };
-  PackedIn<W> in;
+  // The lane's sign words stay in registers for bf16 outputs of long
+  // launches (fp32 outputs would spill with them).
+  constexpr bool kRegSigns = !SHORT && !F32 && !ROT;
+  uint32_t S_l[kRegSigns ? 16 : 1];
+  if constexpr (kRegSigns) load_sign_words(s_sign, l, S_l);
+  const uint32_t* signs = kRegSigns ? static_cast<const uint32_t*>(S_l) : static_cast<const uint32_t*>(s_sign);
+  // Step k takes item gw + k * n_warps, a V item when (item ^ k) is odd.
+  PackedIn<W> in, in2;
   int step = 0;
-  if (gw < items) load_packed_item<M::B, VB>(p, ((gw ^ step) & 1) != 0, item_irow(gw), l, in);
+  if (gw < items) load_packed_item<M::B, VB>(p, (gw & 1) != 0, item_irow(gw), l, in);
+  if constexpr (SHORT) {
+    const int it1 = gw + n_warps;
+    if (it1 < items) load_packed_item<M::B, VB>(p, ((it1 ^ 1) & 1) != 0, item_irow(it1), l, in2);
+  }
   for (int it = gw; it < items; it += n_warps, ++step) {
     const bool is_v = ((it ^ step) & 1) != 0;
     const int r0 = (it >> 1) * G::RPW + sub;
@@ -719,19 +751,24 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
     const int r = valid ? r0 : p.rows - 1;
     const size_t out_off = static_cast<size_t>(r) * D + kGroup * l;
 
-    const int nx = it + n_warps;
-    // the next item's loads are issued once this item's inputs are consumed
+    // the loads of step + kAhead are issued once this item's inputs are consumed
+    const int nx = it + kAhead * n_warps;
     auto prefetch = [&]() {
-      if (nx < items) load_packed_item<M::B, VB>(p, ((nx ^ (step + 1)) & 1) != 0, item_irow(nx), l, in);
+      if constexpr (SHORT) {
+        in = in2;
+        if (nx < items) load_packed_item<M::B, VB>(p, ((nx ^ (step + 2)) & 1) != 0, item_irow(nx), l, in2);
+      } else {
+        if (nx < items) load_packed_item<M::B, VB>(p, ((nx ^ (step + 1)) & 1) != 0, item_irow(nx), l, in);
+      }
     };
     if (!is_v) {
       float x[32];
       decode_key_item<KMODE>(in, x, prefetch);
       if (valid) store_group<F32>(p.k_out, out_off, x);
     } else {
-      decode_value_item<G::LPR, VB, F32, ROT>(in, l, s_sign, s_cent + (CentroidTable<VB>::kRep > 1 ? lane : 0),
-                                              p.rot_scale, p.neg_zero, valid, p.v_out, out_off,
-                                         prefetch);
+      decode_value_item<G::LPR, VB, F32, ROT, kRegSigns>(in, l, signs,
+                                                       s_cent + (CentroidTable<VB>::kRep > 1 ? lane : 0),
+                                                       p.rot_scale, p.neg_zero, valid, p.v_out, out_off, prefetch);
     }
   }
 }
@@ -815,9 +852,13 @@ cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
 
 template <int D, int VB, int KMODE, bool F32, bool ROT>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
-  static const int resident = resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT>);
+  static const int resident = std::min(resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT, false>),
+                                       resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT, true>));
   const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
-  const cudaError_t e = launch_pdl(decode_kernel<D, VB, KMODE, F32, ROT>, grid_for(items, resident), p, s);
+  const int grid = grid_for(items, resident);
+  const bool short_launch = items <= static_cast<long long>(kSnakeSteps) * grid * (kThreads / 32);
+  const cudaError_t e = short_launch ? launch_pdl(decode_kernel<D, VB, KMODE, F32, ROT, true>, grid, p, s)
+                                     : launch_pdl(decode_kernel<D, VB, KMODE, F32, ROT, false>, grid, p, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -866,12 +907,6 @@ cudaError_t launch_decode_dt(const DecodeParams& p, int v_bits, cudaStream_t s) 
 }
 
 
-template <int D>
-cudaError_t launch_decode(const DecodeParams& p, int v_bits, bool out_bf16, bool rotated_v, cudaStream_t s) {
-  if (rotated_v)
-    return out_bf16 ? launch_decode_dt<D, false, true>(p, v_bits, s) : launch_decode_dt<D, true, true>(p, v_bits, s);
-  return out_bf16 ? launch_decode_dt<D, false, false>(p, v_bits, s) : launch_decode_dt<D, true, false>(p, v_bits, s);
-}
 
 // ---------------------------------------------------------------------------
 // unrotateValues: the inverse rotation (Hadamard transform, then signs) of
