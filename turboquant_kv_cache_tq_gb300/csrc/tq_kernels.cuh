@@ -361,13 +361,20 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
 // V encode of the group held by this lane (the whole row's lanes rotate together).
 // REP: s_cells is the lane's replica of the compact cell table (bytes, see
 // RepCells) and the rare masked path reads the full table from global memory.
-template <int LPR, int VB, bool F32, bool REP, typename Prefetch>
+// SIGNS_IN_REGS: s_sign is the lane's own 16 sign words (held in registers by
+// the caller) instead of the block's shared table.
+template <int LPR, int VB, bool F32, bool REP, bool SIGNS_IN_REGS, typename Prefetch>
 __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const uint32_t* s_sign,
                                                   const void* s_cells, float rot_scale, float neg_zero,
                                                   bool store, uint8_t* codes, uint16_t* scale_out,
                                                   Prefetch&& prefetch) {
   uint32_t S[16];
-  load_sign_words(s_sign, l, S);
+  if constexpr (SIGNS_IN_REGS) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) S[j] = s_sign[j];
+  } else {
+    load_sign_words(s_sign, l, S);
+  }
   float2 Y[16];
   if constexpr (F32) {
 #pragma unroll
@@ -468,6 +475,14 @@ __global__ void __launch_bounds__(EncodeShape<VB, F32, ALLOW_REP>::kBlockThreads
     }
     cp_async_commit();
   };
+  // The wide (512-thread, replicated-table) shape keeps each lane's sign
+  // words in registers for the whole launch: 16 fewer shared-memory
+  // wavefronts per V item (long-context v8 encode 320 -> 310 us). The
+  // 256-thread shapes would spill with them and measured slower.
+  constexpr bool kRegSigns = SH::REP;
+  uint32_t S_l[kRegSigns ? 16 : 1];
+  if constexpr (kRegSigns) load_sign_words(s_sign, l, S_l);
+  const uint32_t* signs = kRegSigns ? static_cast<const uint32_t*>(S_l) : static_cast<const uint32_t*>(s_sign);
   issue(0);
   cp_async_wait<0>();
 #pragma unroll
@@ -496,7 +511,7 @@ __global__ void __launch_bounds__(EncodeShape<VB, F32, ALLOW_REP>::kBlockThreads
       encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l,
                                   p.k_scales + orow * NG + l, p.k_zeros + orow * NG + l, no_prefetch);
     } else {
-      encode_value_item<G::LPR, VB, F32, SH::REP>(in, l, s_sign, cells, p.rot_scale, p.neg_zero, valid,
+      encode_value_item<G::LPR, VB, F32, SH::REP, kRegSigns>(in, l, signs, cells, p.rot_scale, p.neg_zero, valid,
                                          p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l,
                                          no_prefetch);
     }
