@@ -582,18 +582,62 @@ def copy_floor(dev, reps: int):
     print("copy floor (32 x 11.67 MB copies in a CUDA graph): %.2f us per launch, %.0f GB/s" % (us, 23330816 / us / 1e3))
 
 
+def host_link_floor(dev, reps: int):
+    """The e2e step's copies alone: 32 layers' K, V (16.78 MB each layer) from
+    pinned host memory to the device and the same bytes back, uploads and
+    downloads on two streams at once, as run_e2e issues them; and each
+    direction alone."""
+    nb = 16777216 // 2
+    hs = [torch.zeros(nb, dtype=torch.int16).pin_memory() for _ in range(32)]
+    ho = [torch.empty(nb, dtype=torch.int16).pin_memory() for _ in range(32)]
+    ds = [torch.empty(nb, dtype=torch.int16, device=dev) for _ in range(32)]
+    do = [torch.zeros(nb, dtype=torch.int16, device=dev) for _ in range(32)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    total = 32 * nb * 2
+
+    def timed(up: bool, down: bool) -> float:
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        main = torch.cuda.current_stream(dev)
+        e0.record(main)
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        for _ in range(reps):
+            for i in range(32):
+                if up:
+                    with torch.cuda.stream(s_in):
+                        ds[i].copy_(hs[i], non_blocking=True)
+                if down:
+                    with torch.cuda.stream(s_out):
+                        ho[i].copy_(do[i], non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+        e1.record(main)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    timed(True, True)
+    for up, down, what in ((True, False, "host->device"), (False, True, "device->host"), (True, True, "both at once")):
+        ms = timed(up, down)
+        print("host link, %s: %.2f ms per 32 layers, %.0f GB/s per direction" % (what, ms, total / ms / 1e6))
+
+
 def run_case(name: str, reps: int):
     """A small fixed case for profiling one kernel with ncu: the codec on one
     workload (encode then decode, `reps` times), one fused decode-attention
     step over the long-context cache shape, or the plain-copy floor of the
-    Llama-3-8B-shaped layer ('copy_floor'). Prints the median timing; it is
-    not a bench line."""
+    Llama-3-8B-shaped layer ('copy_floor'), or the pinned host copies of the
+    e2e step alone ('host_link'). Prints the median timing; it is not a bench
+    line."""
     import turboquant_kv_cache_tq_gb300 as tq
     from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv
 
     dev = torch.device("cuda")
     if name == "copy_floor":
         copy_floor(dev, max(reps, 20))
+        return
+    if name == "host_link":
+        host_link_floor(dev, max(reps, 3))
         return
     e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
     if name == "attention":
@@ -646,7 +690,7 @@ def main(argv=None):
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the secondary long-context / hd256 / hd512 measurements")
     ap.add_argument("--case", default=None,
-                    help="profiling aid: run one small case (a workload name, 'attention' or 'copy_floor') --reps times")
+                    help="profiling aid: run one small case (a workload name, 'attention', 'copy_floor' or 'host_link') --reps times")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     if args.case:
