@@ -88,10 +88,12 @@ struct EncodeRing {
 // restricted to the cells a finite-RMS group can reach: |v| <= sqrt(32), so
 // cells OFF - R .. OFF + R with R = floor(5.6569 S) + 1 (23 and 93 KB), in one
 // 512-thread block per SM beside a 4-stage ring. Narrower tables conflict
-// less and the extra register would spill at three 256-thread blocks per SM,
-// so those shapes and fp32 inputs keep the shared single table (measured on
-// the long-context cache: v8 encode 393 -> 299 us, v3 302 -> 333 us if
-// replicated too).
+// less: at head_dim 64 and 128 their shapes keep the shared single table in
+// three 256-thread blocks per SM (long-context cache: v8 encode 393 -> 299 us
+// replicated, v3 302 -> 333 us if replicated too); at head_dim 256 and 512,
+// whose rows need three and four cross-lane butterfly stages, the wide shape
+// is faster at every width (hd256 v4 encode 68 -> 58 us, hd512 v2 67 -> 59 us
+// in one ablation run). fp32 inputs keep the single table.
 #ifndef TQ_ENCODE_REP_THREADS
 #define TQ_ENCODE_REP_THREADS 512
 #endif
@@ -122,9 +124,9 @@ static_assert(rep_range_holds_all_boundaries<2>() && rep_range_holds_all_boundar
 // item, which only pays off on launches of many rows; smaller launches (for
 // instance decode-step appends) take the single-table shape.
 constexpr int kRepMinRows = 65536;
-template <int VB, bool F32, bool ALLOW_REP = true>
+template <int D, int VB, bool F32, bool ALLOW_REP = true>
 struct EncodeShape {
-  static constexpr bool REP = ALLOW_REP && !F32 && VB >= 5;
+  static constexpr bool REP = ALLOW_REP && !F32 && (VB >= 5 || D >= 256);
   static constexpr bool WIDE = REP;
   static constexpr int kBlockThreads = WIDE ? TQ_ENCODE_REP_THREADS : kThreads;
   static constexpr int kMinBlocks = WIDE ? 1 : kEncodeMinBlocks;
@@ -414,12 +416,12 @@ __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const 
 }
 
 template <int D, int VB, int KMODE, bool F32, bool ALLOW_REP, bool SNAKE>
-__global__ void __launch_bounds__(EncodeShape<VB, F32, ALLOW_REP>::kBlockThreads,
-                                  EncodeShape<VB, F32, ALLOW_REP>::kMinBlocks)
+__global__ void __launch_bounds__(EncodeShape<D, VB, F32, ALLOW_REP>::kBlockThreads,
+                                  EncodeShape<D, VB, F32, ALLOW_REP>::kMinBlocks)
     encode_kernel(EncodeParams p) {
   using G = Geo<D>;
   using M = KeySpec<KMODE>;
-  using SH = EncodeShape<VB, F32, ALLOW_REP>;
+  using SH = EncodeShape<D, VB, F32, ALLOW_REP>;
   constexpr int NC = SH::REP ? 1 : CellGrid<VB>::NC;
   constexpr int pdk = D * M::B / 8;
   constexpr int pdv = D * VB / 8;
@@ -830,7 +832,7 @@ inline cudaError_t launch_pdl(void (*kernel)(Params), int grid, const Params& p,
 
 template <int D, int VB, int KMODE, bool F32, bool ALLOW_REP, bool SNAKE>
 cudaError_t launch_encode_shape(const EncodeParams& p, cudaStream_t s, int grid) {
-  using SH = EncodeShape<VB, F32, ALLOW_REP>;
+  using SH = EncodeShape<D, VB, F32, ALLOW_REP>;
   const cudaError_t e =
       launch_pdl(encode_kernel<D, VB, KMODE, F32, ALLOW_REP, SNAKE>, grid, p, s, SH::kSmem, SH::kBlockThreads);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -840,7 +842,7 @@ cudaError_t launch_encode_shape(const EncodeParams& p, cudaStream_t s, int grid)
 // dynamic shared memory first), computed once per instantiation.
 template <int D, int VB, int KMODE, bool F32, bool ALLOW_REP, bool SNAKE>
 int encode_resident() {
-  using SH = EncodeShape<VB, F32, ALLOW_REP>;
+  using SH = EncodeShape<D, VB, F32, ALLOW_REP>;
   static const int resident =
       prepare_dyn_smem(encode_kernel<D, VB, KMODE, F32, ALLOW_REP, SNAKE>, SH::kSmem, SH::kBlockThreads);
   return resident;
@@ -849,14 +851,14 @@ int encode_resident() {
 template <int D, int VB, int KMODE, bool F32>
 cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
   const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
-  if constexpr (EncodeShape<VB, F32, true>::REP) {
+  if constexpr (EncodeShape<D, VB, F32, true>::REP) {
     if (p.rows >= kRepMinRows) {
-      constexpr int threads = EncodeShape<VB, F32, true>::kBlockThreads;
+      constexpr int threads = EncodeShape<D, VB, F32, true>::kBlockThreads;
       const int grid = grid_for(items, encode_resident<D, VB, KMODE, F32, true, false>(), threads);
       return launch_encode_shape<D, VB, KMODE, F32, true, false>(p, s, grid);
     }
   }
-  constexpr int threads = EncodeShape<VB, F32, false>::kBlockThreads;
+  constexpr int threads = EncodeShape<D, VB, F32, false>::kBlockThreads;
   const int resident = std::min(encode_resident<D, VB, KMODE, F32, false, false>(),
                                 encode_resident<D, VB, KMODE, F32, false, true>());
   const int grid = grid_for(items, resident, threads);
