@@ -87,13 +87,14 @@ struct EncodeRing {
 // lane L at 16 r + L % 16: the 16 lanes of a half-warp never share a bank),
 // restricted to the cells a finite-RMS group can reach: |v| <= sqrt(32), so
 // cells OFF - R .. OFF + R with R = floor(5.6569 S) + 1 (23 and 93 KB), in one
-// 512-thread block per SM beside a 4-stage ring. Narrower tables conflict
-// less: at head_dim 64 and 128 their shapes keep the shared single table in
-// three 256-thread blocks per SM (long-context cache: v8 encode 393 -> 299 us
-// replicated, v3 302 -> 333 us if replicated too); at head_dim 256 and 512,
-// whose rows need three and four cross-lane butterfly stages, the wide shape
-// is faster at every width (hd256 v4 encode 68 -> 58 us, hd512 v2 67 -> 59 us
-// in one ablation run). fp32 inputs keep the single table.
+// 512-thread block per SM beside a 4-stage ring (which also holds each
+// lane's sign words in registers). Narrower tables conflict less, but from
+// head_dim 128 up the wide shape is faster at every width too (ablation runs:
+// [32,8,8192,128] v3 encode 322 -> 301 us, hd256 v4 68 -> 58 us, hd512 v2
+// 67 -> 59 us; v8 on the long-context cache 393 -> 299 us when the shape was
+// introduced). Head_dim 64 (one cross-lane stage) keeps the shared single
+// table in three 256-thread blocks per SM for widths below 5, unmeasured
+// against the wide shape; fp32 inputs keep the single table.
 #ifndef TQ_ENCODE_REP_THREADS
 #define TQ_ENCODE_REP_THREADS 512
 #endif
@@ -126,7 +127,7 @@ static_assert(rep_range_holds_all_boundaries<2>() && rep_range_holds_all_boundar
 constexpr int kRepMinRows = 65536;
 template <int D, int VB, bool F32, bool ALLOW_REP = true>
 struct EncodeShape {
-  static constexpr bool REP = ALLOW_REP && !F32 && (VB >= 5 || D >= 256);
+  static constexpr bool REP = ALLOW_REP && !F32 && (VB >= 5 || D >= 128);
   static constexpr bool WIDE = REP;
   static constexpr int kBlockThreads = WIDE ? TQ_ENCODE_REP_THREADS : kThreads;
   static constexpr int kMinBlocks = WIDE ? 1 : kEncodeMinBlocks;
