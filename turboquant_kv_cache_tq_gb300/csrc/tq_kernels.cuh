@@ -86,7 +86,7 @@ struct EncodeRing {
 // shapes (bf16 inputs) keep the table once per half-warp lane (entry r for
 // lane L at 16 r + L % 16: the 16 lanes of a half-warp never share a bank),
 // restricted to the cells a finite-RMS group can reach: |v| <= sqrt(32), so
-// cells OFF - R .. OFF + R with R = floor(5.6569 S) + 1 (23 and 91 KB), in one
+// cells OFF - R .. OFF + R with R = floor(5.6569 S) + 1 (23 and 93 KB), in one
 // 512-thread block per SM beside a 4-stage ring (which also holds each
 // lane's sign words in registers). Narrower tables conflict less, but from
 // head_dim 128 up the wide shape is faster at every width too (ablation runs:
