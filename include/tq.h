@@ -66,7 +66,8 @@ int64_t tq_packed_dim(int64_t dim, int bits);
  *   k_codes, k_scales, k_zeros, v_codes, v_scales: the packed cache, capacity
  *               t_cap tokens; tokens [t_off, t_off + T) are written, nothing
  *               else is touched.
- * T == 0 (or B*H == 0) is a no-op that returns TQ_OK. */
+ * T == 0 (or B*H == 0) is a no-op that returns TQ_OK. B*H*T above
+ * 2^31 - 1 - 2^24 rows returns TQ_ERR_INVALID_ARG (as for tq_decode_kv). */
 tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
                        int64_t B, int64_t H, int64_t T, int64_t D,
                        int k_bits, int k_signed, int v_bits,
@@ -106,7 +107,7 @@ tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const 
  * and store in the same dtype. x and out are device pointers, 16-byte
  * aligned, [n_rows, D], and must not overlap (the input is read through
  * the read-only data path).
- * D in {64,128,256,512}; n_rows == 0 is a no-op; n_rows < 2^31 - 64. */
+ * D in {64,128,256,512}; n_rows == 0 is a no-op; n_rows <= 2^31 - 1 - 2^24. */
 tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, void* out, void* stream);
 
 /* Lloyd-Max index (ops.ts, searchsorted): idx[i] = number of boundaries of

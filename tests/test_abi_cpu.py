@@ -112,6 +112,11 @@ def test_misaligned_buffers_rejected(L):
 def test_size_overflow_rejected(L):
     assert _enc(L, B=1 << 20, H=1 << 20, T=1 << 12) == INVALID
     assert _dec(L, T=1 << 31, t_cap=1 << 31) == INVALID
+    # rows just past 2^31 - 1 - 2^24 (kernel item indices keep 2^24 of headroom)
+    over = (1 << 31) - (1 << 24)
+    assert _enc(L, H=1, T=over, t_cap=over) == INVALID
+    assert _dec(L, H=1, T=over, t_cap=over) == INVALID
+    assert L.tq_unrotate(1 << 20, 0, over, 128, 1 << 21, None) == INVALID
 
 
 def test_unrotate_checks(L):

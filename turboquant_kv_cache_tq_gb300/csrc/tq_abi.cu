@@ -84,7 +84,9 @@ tq_status check_common(int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap
   if (bh > 0 && T > lim / bh) return TQ_ERR_INVALID_ARG;
   if (bh > 0 && t_cap > (1LL << 62) / (bh * 512)) return TQ_ERR_INVALID_ARG;
   *rows = bh * T;
-  if (*rows > lim - 64) return TQ_ERR_INVALID_ARG;  // tile arithmetic stays in int
+  // Item indices, including those a warp computes a few steps past the end
+  // (its prefetches), stay in int with 2^24 to spare.
+  if (*rows > lim - (1LL << 24)) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
 
@@ -218,7 +220,7 @@ extern "C" tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, 
   if (n_rows < 0) return TQ_ERR_INVALID_ARG;
   if (!head_dim_ok(D)) return TQ_ERR_HEAD_DIM;
   if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_DTYPE;
-  if (n_rows > 0x7fffffffLL - 64) return TQ_ERR_INVALID_ARG;
+  if (n_rows > 0x7fffffffLL - (1LL << 24)) return TQ_ERR_INVALID_ARG;  // as in check_common
   if (n_rows == 0) return TQ_OK;
   if (!x || !out) return TQ_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGNMENT;
