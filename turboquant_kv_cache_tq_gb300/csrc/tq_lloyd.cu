@@ -7,9 +7,10 @@
 // every centroid becomes the mean of its cell (a cell with no samples keeps
 // its centroid).
 //
-// One launch per iteration. Each block bins a fixed slice of the sample by
-// binary search over the boundaries (shared memory, padded with +Inf to a
-// power of two) into per-warp shared histograms, then adds its per-cell
+// One launch per iteration. Each block bins a fixed slice of the sample
+// (loaded eight samples per thread at a time) by binary search over the
+// boundaries (shared memory, padded with +Inf to a power of two) into
+// per-warp shared histograms, then adds its per-cell
 // counts and sums into global totals with integer atomics. Sums are int64
 // fixed point in units of 2^-32: every sample of magnitude >= 2^-9 is exact
 // there (smaller ones are rounded to the unit), so the totals are exact and do
@@ -29,6 +30,7 @@ namespace {
 constexpr int kLloydThreads = 256;
 constexpr int kLloydWarps = kLloydThreads / 32;
 constexpr int kLloydBlocksPerSm = 2;
+constexpr int kLloydBatch = 8;
 constexpr double kFixedScale = 4294967296.0;  // 2^32
 
 struct LloydParams {
@@ -62,14 +64,27 @@ __global__ void __launch_bounds__(kLloydThreads) lloyd_iter_kernel(LloydParams p
   __syncthreads();
   const long long lo = static_cast<long long>(blockIdx.x) * p.n / gridDim.x;
   const long long hi = static_cast<long long>(blockIdx.x + 1) * p.n / gridDim.x;
-  for (long long i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-    const float x = p.x[i];
-    int cell = 0;  // count(boundaries < x): boundaries ascend, padding is +Inf
-    for (int step = K >> 1; step > 0; step >>= 1)
-      if (s_b[cell + step - 1] < x) cell += step;
-    atomicAdd(reinterpret_cast<unsigned long long*>(&s_sum[warp][cell]),
-              static_cast<unsigned long long>(__float2ll_rn(__fmul_rn(x, 4294967296.0f))));
-    atomicAdd(&s_cnt[warp][cell], 1u);
+  // A thread loads kLloydBatch samples before binning any of them, so their
+  // reads overlap instead of each waiting out its own latency; the totals
+  // are exact integers, so the order of the additions does not matter.
+  for (long long base = lo + threadIdx.x; base < hi; base += kLloydBatch * static_cast<long long>(blockDim.x)) {
+    float xs[kLloydBatch];
+#pragma unroll
+    for (int u = 0; u < kLloydBatch; ++u) {
+      const long long i = base + static_cast<long long>(u) * blockDim.x;
+      xs[u] = i < hi ? p.x[i] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kLloydBatch; ++u) {
+      if (base + static_cast<long long>(u) * blockDim.x >= hi) break;
+      const float x = xs[u];
+      int cell = 0;  // count(boundaries < x): boundaries ascend, padding is +Inf
+      for (int step = K >> 1; step > 0; step >>= 1)
+        if (s_b[cell + step - 1] < x) cell += step;
+      atomicAdd(reinterpret_cast<unsigned long long*>(&s_sum[warp][cell]),
+                static_cast<unsigned long long>(__float2ll_rn(__fmul_rn(x, 4294967296.0f))));
+      atomicAdd(&s_cnt[warp][cell], 1u);
+    }
   }
   __syncthreads();
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
