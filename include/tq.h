@@ -246,12 +246,14 @@ tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H
  *              boundaries: levels - 1 fp32 (device), the final midpoints.
  *   workspace  device scratch of tq_lloyd_max_fit_workspace_size(levels)
  *              bytes (16-byte aligned; the call clears it first).
- * One kernel is enqueued per iteration; n < 2^31. */
+ * One cooperative kernel runs every iteration (its blocks meet at a bounded
+ * grid barrier per iteration; if a wait gives up, centroids and boundaries
+ * are left NaN); n < 2^31. */
 tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
                            float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
                            void* stream);
 
-/* Bytes of scratch tq_lloyd_max_fit needs (16 + 16 * levels), or
+/* Bytes of scratch tq_lloyd_max_fit needs (64 + 48 * levels), or
  * -TQ_ERR_INVALID_ARG for a level count that is not a power of two in
  * [2, 256]. */
 int64_t tq_lloyd_max_fit_workspace_size(int levels);

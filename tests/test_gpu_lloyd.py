@@ -89,3 +89,16 @@ def test_bench_size_fit():
     c, b = _fit(x, init, 500)
     rc, rb = lf.lloyd_max_fit(x, init, 500)
     assert np.max(_ulps(c, rc)) <= 4 and np.max(_ulps(b, rb)) <= 4
+
+
+def test_large_sample_takes_the_int64_sums():
+    """A warp keeps its cell sums in split 32-bit words while it bins at most
+    65536 samples per iteration; 170 M samples (more than 65536 per warp at
+    two blocks of eight warps on each of 152 SMs) take the int64 sums.
+    Two iterations against the oracle."""
+    n = 170_000_000
+    x = np.random.default_rng(11).standard_normal(n).astype(np.float32)
+    init = np.linspace(-2.5, 2.5, 16).astype(np.float32)
+    c, b = _fit(x, init, 2)
+    rc, rb = lf.lloyd_max_fit(x, init, 2)
+    assert np.max(_ulps(c, rc)) <= 4 and np.max(_ulps(b, rb)) <= 4
