@@ -157,14 +157,19 @@ def check_roundtrip(k, v, k_bits, k_signed, v_bits, t_cap=None, t_off=0):
             inexact += compare_decoded(vg.cpu().numpy(), vr, "V decode")
         else:
             kf, vf = oracle.decode_kv(rcache, Td, k_bits, k_signed, v_bits, out_dtype=oracle.F32)
-            for gt, rt, rf, name in ((kg, kr, kf, "K bf16"), (vg, vr, vf, "V bf16")):
-                gb = gt.cpu().view(torch.int16).numpy().view(np.uint16)
-                if not np.array_equal(gb, rt):
-                    # allowed only where the fp32 results already differ within tolerance
-                    gf = oracle.bf16_bits_to_f32(gb)
-                    rbf = oracle.bf16_bits_to_f32(rt)
-                    nan = np.isnan(rbf)
-                    assert np.array_equal(np.isnan(gf), nan), name
-                    d = np.abs(gf[~nan].astype(np.float64) - rbf[~nan])
-                    assert np.all(d <= 2.0 ** -7 * np.abs(rf[~nan]) + 1e-30), name
+            compare_decoded_bf16(kg.cpu().view(torch.int16).numpy().view(np.uint16), kr, kf, "K bf16")
+            compare_decoded_bf16(vg.cpu().view(torch.int16).numpy().view(np.uint16), vr, vf, "V bf16")
     return n_exc, inexact
+
+
+def compare_decoded_bf16(gpu_bits: np.ndarray, ref_bits: np.ndarray, ref_f32: np.ndarray, what: str):
+    """bf16 outputs: equal to the oracle's bf16 bits, except where the fp32
+    results already differ within the decode tolerance (then one bf16 step)."""
+    if np.array_equal(gpu_bits, ref_bits):
+        return
+    gf = oracle.bf16_bits_to_f32(gpu_bits)
+    rbf = oracle.bf16_bits_to_f32(ref_bits)
+    nan = np.isnan(rbf)
+    assert np.array_equal(np.isnan(gf), nan), what
+    d = np.abs(gf[~nan].astype(np.float64) - rbf[~nan])
+    assert np.all(d <= 2.0 ** -7 * np.abs(ref_f32[~nan]) + 1e-30), what

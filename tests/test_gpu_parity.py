@@ -14,7 +14,7 @@ import oracle
 import turboquant_kv_cache_tq_gb300 as tq
 from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_append_steps, make_kv, to_oracle
 from tests.gpu_common import (cache_from_numpy, cache_to_numpy, check_roundtrip, compare_decoded,
-                              compare_encoded, gpu_encode, oracle_encode, require_gpu)
+                              compare_decoded_bf16, compare_encoded, gpu_encode, oracle_encode, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -100,9 +100,18 @@ def test_workload_full_size_sampled(name):
         # the oracle decodes the same packed bytes (a value index may differ
         # from the oracle's encode inside the boundary band)
         kr, vr = oracle.decode_kv(g, len(rows), w.k_bits, w.k_signed, vb)
-        compare_decoded(kd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), kr.reshape(-1, D), "K")
-        compare_decoded(vd.reshape(-1, D)[torch.from_numpy(rows).cuda()].cpu().numpy(), vr.reshape(-1, D), "V")
-        del gcache, kd, vd
+        sel = torch.from_numpy(rows).cuda()
+        compare_decoded(kd.reshape(-1, D)[sel].cpu().numpy(), kr.reshape(-1, D), "K")
+        compare_decoded(vd.reshape(-1, D)[sel].cpu().numpy(), vr.reshape(-1, D), "V")
+        del kd, vd
+        # bf16 outputs, as the bench decodes them
+        kb16, vb16 = tq.tq_decode_kv(gcache, w.T, w.k_bits, w.k_signed, vb, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        kr16, vr16 = oracle.decode_kv(g, len(rows), w.k_bits, w.k_signed, vb, out_dtype=oracle.BF16)
+        _bits = lambda t: t.reshape(-1, D)[sel].cpu().view(torch.int16).numpy().view(np.uint16)
+        compare_decoded_bf16(_bits(kb16), kr16.reshape(-1, D), kr.reshape(-1, D), "K bf16")
+        compare_decoded_bf16(_bits(vb16), vr16.reshape(-1, D), vr.reshape(-1, D), "V bf16")
+        del gcache, kb16, vb16
         torch.cuda.empty_cache()
 
 
@@ -141,7 +150,15 @@ def test_long_launches_sampled(D, dtype):
         sel = torch.from_numpy(rows).cuda()
         compare_decoded(kd.reshape(-1, D)[sel].cpu().numpy(), kref.reshape(-1, D), "K")
         compare_decoded(vd.reshape(-1, D)[sel].cpu().numpy(), vref.reshape(-1, D), "V")
-        del cache, kd, vd
+        del kd, vd
+        # bf16 outputs (long launches keep each lane's sign words in registers there)
+        kb16, vb16 = tq.tq_decode_kv(cache, T, kb, ks, vb, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        kr16, vr16 = oracle.decode_kv(got, len(rows), kb, ks, vb, out_dtype=oracle.BF16)
+        _bits = lambda t: t.reshape(-1, D)[sel].cpu().view(torch.int16).numpy().view(np.uint16)
+        compare_decoded_bf16(_bits(kb16), kr16.reshape(-1, D), kref.reshape(-1, D), "K bf16")
+        compare_decoded_bf16(_bits(vb16), vr16.reshape(-1, D), vref.reshape(-1, D), "V bf16")
+        del cache, kb16, vb16
     torch.cuda.empty_cache()
 
 
