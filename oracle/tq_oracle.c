@@ -233,10 +233,20 @@ int oracle_encode_keys_row(const float* x, int d, int bits, int is_signed,
     const int max_val = is_signed ? (1 << (bits - 1)) - 1 : (1 << bits) - 1;
     for (int g = 0; g < d / GROUP; g++) {
         const float* xg = x + g * GROUP;
+        /* ops.minAxis / ops.maxAxis. A NaN anywhere in the group makes both
+         * NaN (the reductions propagate NaN, as IEEE 754-2019 minimum and
+         * maximum do); otherwise a left-to-right scan that keeps the first of
+         * equal values (only +0 / -0 can tell). */
         float mn = xg[0], mx = xg[0];
+        int has_nan = 0;
+        for (int i = 0; i < GROUP; i++) has_nan |= (xg[i] != xg[i]);
         for (int i = 1; i < GROUP; i++) {
             if (xg[i] < mn) mn = xg[i];
             if (xg[i] > mx) mx = xg[i];
+        }
+        if (has_nan) {
+            mn = NAN;
+            mx = NAN;
         }
         float scale, zp, lo, hi;
         if (is_signed) {
@@ -262,7 +272,9 @@ int oracle_encode_keys_row(const float* x, int d, int bits, int is_signed,
             float r = oracle_round(shifted);
             if (r < lo) r = lo;
             if (r > hi) r = hi;
-            int q = (int)r;
+            /* astype(int8 / uint8): clip keeps a NaN, which converts to 0 (the
+             * reading taken for a conversion IEEE leaves invalid). */
+            int q = (r != r) ? 0 : (int)r;
             codes[g * GROUP + i] = (uint8_t)(q & 0xFF); /* int8 two's complement */
         }
         scales[g] = oracle_f32_to_f16(scale);

@@ -51,6 +51,94 @@ def test_constant_key_group_gives_zero_scale_and_infinite_zero(oracle_mod, bits,
     assert np.all(np.isnan(dec[0, :32])) and np.all(np.isfinite(dec[0, 32:]))
 
 
+def _f16_nan(h):
+    return (int(h) & 0x7C00) == 0x7C00 and (int(h) & 0x03FF) != 0
+
+
+# ---- keys and values with Inf / NaN: the IEEE special cases of the page's formulas ----
+@pytest.mark.parametrize("bits,signed", KEY_MODES)
+@pytest.mark.parametrize("pos", [0, 17, 31])
+def test_key_group_with_nan(oracle_mod, bits, signed, pos):
+    """A NaN anywhere in a group (also first, where a plain < scan would keep
+    it, and last) makes min and max NaN: scale, zero point and every quotient
+    are NaN and every code converts to 0; the other group is untouched."""
+    x = RNG.standard_normal((1, 64)).astype(np.float32)
+    c0, s0, z0 = oracle_mod.encode_keys(x, bits, signed)
+    x[0, pos] = np.nan
+    codes, sc, zr = oracle_mod.encode_keys(x, bits, signed)
+    assert np.all(codes[0, :32] == 0)
+    assert _f16_nan(sc[0, 0]) and _f16_nan(zr[0, 0])
+    assert np.array_equal(codes[0, 32:], c0[0, 32:]) and sc[0, 1] == s0[0, 1] and zr[0, 1] == z0[0, 1]
+    dec = oracle_mod.decode_keys(codes, sc, zr, signed)
+    assert np.all(np.isnan(dec[0, :32])) and np.all(np.isfinite(dec[0, 32:]))
+
+
+@pytest.mark.parametrize("bits,signed", KEY_MODES)
+@pytest.mark.parametrize("lo", [-1.0, 0.5])
+def test_key_group_with_positive_inf(oracle_mod, bits, signed, lo):
+    """max = +Inf, min finite: range and scale are +Inf, scale + eps = Inf.
+    Unsigned: zero point round(min / Inf) = a zero with min's sign; signed:
+    (Inf + min) / (2 Inf) = NaN. Every finite x gives x / Inf = +-0, Inf gives
+    NaN, so every code is 0 either way; the decode (0 + zero) * Inf is NaN."""
+    x = np.linspace(lo, 1.0, 32, dtype=np.float32)[None]
+    x[0, 5] = np.inf
+    codes, sc, zr = oracle_mod.encode_keys(x, bits, signed)
+    assert sc[0, 0] == 0x7C00
+    if signed:
+        assert _f16_nan(zr[0, 0])
+    else:
+        assert zr[0, 0] == (0x8000 if lo < 0 else 0x0000)
+    assert np.all(codes == 0)
+    assert np.all(np.isnan(oracle_mod.decode_keys(codes, sc, zr, signed)))
+
+
+@pytest.mark.parametrize("bits,signed", KEY_MODES)
+def test_key_group_with_both_infinities_or_overflowing_range(oracle_mod, bits, signed):
+    """-Inf and +Inf: range +Inf, and the zero point's numerator (-Inf, or
+    -Inf + Inf) makes it NaN. A finite group +-3e38 overflows the range to
+    +Inf: the signed zero point is round(0 / Inf) = 0, the unsigned one
+    round(-3e38 / Inf) = -0; all codes 0."""
+    x = np.zeros((2, 32), np.float32)
+    x[0] = np.linspace(-1, 1, 32)
+    x[0, 3], x[0, 20] = np.inf, -np.inf
+    x[1, 0::2], x[1, 1::2] = 3e38, -3e38
+    codes, sc, zr = oracle_mod.encode_keys(x, bits, signed)
+    assert sc[0, 0] == 0x7C00 and _f16_nan(zr[0, 0])
+    assert sc[1, 0] == 0x7C00 and zr[1, 0] == (0x0000 if signed else 0x8000)
+    assert np.all(codes == 0)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("bits", [2, 3, 5, 8])
+def test_value_row_with_inf_or_nan(oracle_mod, d, bits):
+    """One Inf (or NaN) in a value row reaches every coordinate of the
+    normalised Hadamard transform, so every group's RMS is Inf (NaN), every
+    normalised value Inf / Inf (NaN / NaN) = NaN, and searchsorted counts no
+    boundary: all indices 0, every scale +Inf (NaN)."""
+    x = RNG.standard_normal((3, d)).astype(np.float32)
+    x[0, 3] = np.inf
+    x[1, d - 1] = np.nan
+    x[2, 11] = -np.inf
+    idx, sc = oracle_mod.encode_values(x, bits)
+    assert np.all(idx == 0)
+    assert np.all(sc[0] == 0x7C00) and np.all(sc[2] == 0x7C00)
+    assert all(_f16_nan(h) for h in sc[1])
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 8])
+def test_value_row_whose_sum_of_squares_overflows(oracle_mod, bits):
+    """One element 1e38 in a row of 128: every rotated coordinate is finite
+    (+-1e38 / sqrt(128)), but 32 squares of ~8.8e36 overflow, so the RMS is
+    +Inf, every normalised value y / Inf is a signed zero and every index is
+    count(boundaries < 0) (a boundary equal to 0 is not below -0 or +0)."""
+    x = np.zeros((1, 128), np.float32)
+    x[0, 7] = 1e38
+    _, b = oracle_mod.lloyd_max(bits)
+    idx, sc = oracle_mod.encode_values(x, bits)
+    assert np.all(sc == 0x7C00)
+    assert np.all(idx == np.count_nonzero(b < 0.0))
+
+
 def test_unsigned_ramp_closed_form(oracle_mod):
     # x_i = i on one group, 5 bits: scale = 31/31 = 1, scale+eps rounds to 1 in
     # fp32, zero point round(0/1) = 0, codes = i exactly
