@@ -352,26 +352,84 @@ def test_lloyd_max_index_at_boundaries(bits):
     assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
 
 
-@pytest.mark.parametrize("D,vb", [(128, 8), (64, 5)])
-def test_wide_tables_with_non_finite_rows(D, vb):
-    """Launches of >= 65536 rows at 5 and 8 bits use the per-lane replicated
-    cell table; a warp holding a row whose RMS is not finite (an Inf input)
-    takes the masked path over the full table instead. Every finite row must
-    still match the oracle, including the rows that share a warp with the
-    Inf rows; the Inf rows' indices are unspecified but in bounds."""
-    B, H, T = 1, 1, 65544
-    g = torch.Generator().manual_seed(77 + vb)
-    k = torch.randn((B, H, T, D), generator=g).to(torch.bfloat16)
-    v = torch.randn((B, H, T, D), generator=g).to(torch.bfloat16)
-    bad = [5, 40000, 65543]
-    for t in bad:
-        v[0, 0, t, 3] = float("inf")
-    gcache = gpu_encode(k, v, 8, True, vb)
-    rpw = 32 // (D // 32)
-    near = sorted({r for t in bad for r in range((t // rpw) * rpw, (t // rpw) * rpw + rpw) if r not in bad and r < T})
-    rows = np.array(sorted(set(near) | set(_sample_rows(T, 300, vb).tolist()) - set(bad)))
-    ko = to_oracle(k).reshape(-1, D)[rows].reshape(1, 1, -1, D)
-    vo = to_oracle(v).reshape(-1, D)[rows].reshape(1, 1, -1, D)
-    ref = oracle.encode_kv(ko, vo, 8, True, vb)
-    got = {key: val.reshape(-1, val.shape[-1])[rows][None, None] for key, val in cache_to_numpy(gcache).items()}
-    compare_encoded(got, ref, D, vb, v_input=vo.reshape(-1, D))
+# ---- non-finite inputs, element by element --------------------------------------------
+# The page's formulas define a result for Inf and NaN inputs too (IEEE
+# arithmetic): a NaN in a key group makes its min, max, scale and zero point
+# NaN and every code 0 (NaN converts to 0); an Inf gives an Inf scale; one Inf
+# or NaN in a value row reaches every rotated coordinate, so the RMS is Inf or
+# NaN, every normalised value is NaN and every index 0 (searchsorted counts
+# nothing below NaN); a finite row whose sum of squares overflows has RMS Inf
+# and normalised values +-0.
+def _k_pattern(x, i):
+    """Plant key pattern i into the 32-element group view x (float32)."""
+    p = i % 10
+    if p == 0:
+        x[0] = float("nan")
+    elif p == 1:
+        x[17] = float("nan")
+    elif p == 2:
+        x[:] = float("nan")
+    elif p == 3:
+        x[5] = float("inf")
+    elif p == 4:
+        x[9] = float("-inf")
+    elif p == 5:
+        x[3], x[20] = float("inf"), float("-inf")
+    elif p == 6:
+        x[:] = float("inf")
+    elif p == 7:
+        x[:] = 3e38
+        x[1::2] = -3e38  # the range overflows
+    elif p == 8:
+        x[:] = 3e38  # range 0; the signed zero point's numerator overflows
+    else:
+        x[:] = x.abs() * 0.25 + 0.5
+        x[7] = float("inf")  # positive minimum: zero point +0
+
+
+def _v_pattern(x, i):
+    """Plant value pattern i into the row view x (float32)."""
+    p = i % 6
+    if p == 0:
+        x[3] = float("inf")
+    elif p == 1:
+        x[x.numel() - 1] = float("nan")
+    elif p == 2:
+        x[0], x[1] = float("inf"), float("-inf")
+    elif p == 3:
+        x[7] = 1e38  # finite rotation, the sum of squares overflows
+    elif p == 4:
+        x[:] = 3e38  # the rotation itself overflows
+    else:
+        x[11] = float("-inf")
+
+
+def _non_finite_kv(B, H, T, D, dtype, seed, n_rows):
+    k = _rand((B, H, T, D), torch.float32, seed)
+    v = _rand((B, H, T, D), torch.float32, seed + 1)
+    R = B * H * T
+    rng = np.random.default_rng(seed)
+    rows = sorted(set([0, R - 1, R // 2] + rng.choice(R, size=min(R, n_rows), replace=False).tolist()))
+    kf, vf = k.view(-1, D), v.view(-1, D)
+    for j, r in enumerate(rows):
+        _k_pattern(kf[r, 32 * (j % (D // 32)): 32 * (j % (D // 32)) + 32], j)
+        _v_pattern(vf[r], j)
+    return k.to(dtype).contiguous(), v.to(dtype).contiguous()
+
+
+@pytest.mark.parametrize("D,vb,dtype,T", [
+    (128, 3, torch.bfloat16, 1000),    # single cell table, 256-thread blocks
+    (64, 2, torch.float32, 777),
+    (256, 4, torch.float32, 301),
+    (512, 5, torch.bfloat16, 129),
+    (128, 8, torch.bfloat16, 65544),   # >= 65536 rows: replicated cell tables (wide shape)
+    (128, 3, torch.bfloat16, 65544),
+    (64, 5, torch.bfloat16, 65544),
+])
+def test_non_finite_rows_match_oracle(D, vb, dtype, T):
+    """Rows holding Inf, NaN and overflowing values, and the rows that share
+    warps with them, match the oracle element by element: codes, scales and
+    zero points (NaN equal to NaN), and decodes."""
+    k, v = _non_finite_kv(1, 1, T, D, dtype, 900 + D + vb + T, 60)
+    for kb, ks in ((8, True), (4, False)):
+        check_roundtrip(k, v, kb, ks, vb)

@@ -80,6 +80,18 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) { return fma2(b, f2(-
 // RN(a * b) that cannot be fused into a consumer; nz must hold a runtime -0.0
 __device__ __forceinline__ float2 mul0(float2 a, float2 b, float2 nz) { return fma2(a, b, nz); }
 
+// min / max that return NaN when either operand is NaN (PTX min.NaN / max.NaN).
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -326,7 +338,9 @@ __device__ __forceinline__ void lm_index2(float2 u, const CellEntry* tab, int& i
 // constant's, without a mask: the caller guarantees |v| * S < OFF, which
 // holds whenever inv is the reciprocal of (a finite group RMS + eps) and y is
 // an element of that group (|y| <= sqrt(32) * rms, so |v * S| <= 5.66 S).
-// MASKED = true is safe for any input (NaN and Inf land in some cell).
+// MASKED = true is safe for any input: NaN and Inf land in some cell, and a
+// value v that is NaN (a group whose RMS is Inf or NaN: an Inf or NaN in the
+// row) gets index 0, since searchsorted counts no boundary below NaN.
 template <int BITS, bool MASKED>
 __device__ __forceinline__ void lm_index2_scaled(float2 y, float inv, const CellEntry* tab, uint32_t& i0,
                                                  uint32_t& i1) {
@@ -345,6 +359,11 @@ __device__ __forceinline__ void lm_index2_scaled(float2 y, float inv, const Cell
   const float2 d = fma2(y, f2(-inv), make_float2(e0.b, e1.b));
   i0 = static_cast<uint32_t>(e0.base) + (__float_as_uint(d.x) >> 31);
   i1 = static_cast<uint32_t>(e1.base) + (__float_as_uint(d.y) >> 31);
+  if constexpr (MASKED) {
+    // s is NaN exactly when v = y * inv is (|v| <= sqrt(32) otherwise)
+    i0 = (s.x != s.x) ? 0u : i0;
+    i1 = (s.y != s.y) ? 0u : i1;
+  }
 }
 
 // Any fp32 value: clamp into the grid first (all boundaries lie inside it, so

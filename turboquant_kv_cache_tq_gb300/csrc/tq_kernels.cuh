@@ -264,13 +264,15 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
   using M = KeySpec<KMODE>;
   float2 X[16];
   float mn, mx;
+  // A NaN anywhere in the group makes both NaN (the page's min / max
+  // reductions propagate it), so the NaN-propagating forms are used.
   if constexpr (F32) {
     mn = __uint_as_float(in.w[0]);
     mx = mn;
 #pragma unroll
     for (int i = 1; i < 32; ++i) {
-      mn = fminf(mn, __uint_as_float(in.w[i]));
-      mx = fmaxf(mx, __uint_as_float(in.w[i]));
+      mn = fmin_nan(mn, __uint_as_float(in.w[i]));
+      mx = fmax_nan(mx, __uint_as_float(in.w[i]));
     }
   } else {
     // min / max on bf16 pairs (exact: the upcast preserves order)
@@ -279,11 +281,11 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
 #pragma unroll
     for (int j = 1; j < 16; ++j) {
       const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&in.w[j]);
-      lo2 = __hmin2(lo2, v2);
-      hi2 = __hmax2(hi2, v2);
+      lo2 = __hmin2_nan(lo2, v2);
+      hi2 = __hmax2_nan(hi2, v2);
     }
-    mn = fminf(__low2float(lo2), __high2float(lo2));
-    mx = fmaxf(__low2float(hi2), __high2float(hi2));
+    mn = fmin_nan(__low2float(lo2), __high2float(lo2));
+    mx = fmax_nan(__low2float(hi2), __high2float(hi2));
   }
   item_to_pairs(in, X);
   prefetch();
@@ -304,14 +306,16 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
   const float se = __fadd_rn(scale, kEps);
   const float inv = __frcp_rn(se);
   // zero point: RN(mn / se), or RN((mx + mn) / (2 se)) = RN((mx + mn) / se) / 2
-  // for signed keys; a quotient that overflows takes IEEE division. The
+  // for signed keys; a quotient that overflows, or a range that is not finite
+  // (an Inf or NaN in the group: se = Inf gives inv = 0 and a NaN remainder,
+  // where num / se is a signed zero or NaN), takes IEEE division. The
   // corrected quotient takes the sign of num (se > 0): for num = -0 the
   // correction's exact zero remainder would otherwise turn -0 into +0, and
   // the fp16 zero point keeps that sign.
   const float num = M::SIGNED ? __fadd_rn(mx, mn) : mn;
   const float zq0 = __fmul_rn(num, inv);
   float zq;
-  if (fabsf(zq0) <= 3.402823466e38f) {
+  if (fabsf(zq0) <= 3.402823466e38f && range <= 3.402823466e38f) {
     zq = copysignf(__fmaf_rn(__fmaf_rn(-zq0, se, num), inv, zq0), num);
     if constexpr (M::SIGNED) zq = __fmul_rn(zq, 0.5f);
   } else {
