@@ -1,27 +1,32 @@
 """Benchmark of the GB300 TurboQuant KV codec: encode + decode throughput.
 
-One step = encode then decode of the KV cache of every layer of a
-Llama-3-8B-shaped model for one 4096-token sequence: 32 layers of K, V
-[1, 8, 4096, 128] bf16 (N(0,1) with 1% outliers x10), keys 8-bit signed,
-values 3-bit. Every layer has its own inputs, packed cache and decoded outputs
-(about 1.3 GB in all, ten times the L2), so each launch streams from HBM.
-The metric is layer-tokens per second: one token = one (batch, position) of
-one layer, all 8 KV heads, K and V, encoded and decoded.
+One step = encode then decode of the whole long-context serving cache: K, V
+[32, 8, 8192, 128] bf16 (N(0, 0.5^2)) into a packed cache of capacity
+8192 + 64 tokens, keys 8-bit signed, values 8-bit, then the decode of the
+8192 tokens back to bf16 (one launch each; 1.66 GB of algorithmic traffic per
+launch, far above the L2). The metric is tokens per second: one token = one
+(sequence, position), all 8 KV heads, K and V, encoded and decoded.
 
 Output: one JSON line (rank 0). Fields beyond the metric:
   roofline      the dominant kernel's algorithmic bytes per launch over its
-                average launch time (CUDA events on its stream), against the
-                measured HBM copy bandwidth (MEASURED_PEAKS.json);
+                average launch time (CUDA events on its stream, inside the
+                timed region), against the measured HBM copy bandwidth
+                (MEASURED_PEAKS.json);
   e2e           the same metric through the Python API with pinned host
-                buffers: host->device copy of the inputs and device->host
-                copy of the decoded K, V inside the timed region;
+                buffers: host->device copy of K, V and device->host copy of
+                the decoded K, V inside the timed region;
   cpu_baseline  the oracle (single-threaded C) on a bounded sample of the
                 same workload, on this machine's host cores;
+  secondary     the other configurations, each with its own roofline: the
+                long-context cache at 3-bit values, the Llama-3-8B-shaped
+                layer (32 layers per step in CUDA graphs), head_dim 256 and
+                512, decode-step appends, fused decode attention, the
+                continuous-batching merge and the Lloyd-Max fit;
   clocks        nvidia-smi samples taken during the timed region.
-``--impl reference`` times the oracle alone as the reference arm.
-Multi-GPU (torchrun): every rank runs an independent replica of the workload
-(weak scaling; the codec has no cross-row exchange), timed between barriers,
-max over ranks.
+``--impl reference`` times the oracle alone as the reference arm, on the
+same configuration. Multi-GPU (torchrun): every rank runs an independent
+replica of the workload (weak scaling; the codec has no cross-row exchange),
+timed between barriers, max over ranks.
 """
 from __future__ import annotations
 
@@ -40,11 +45,29 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-LAYERS = 32
-WORKLOAD = "llama3_8b_layer"
+HEADLINE = "long_context"  # the largest single-GPU configuration
+HEADLINE_V_BITS = 8
+LAYERS = 32  # Llama-3-8B-shaped model: layers per secondary step
 METRIC = "TurboQuant KV encode/decode tokens/s; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+E2E_CHUNK = 4  # sequences per pipelined chunk of the end-to-end step
+
+
+def r4(x):
+    """x to four significant digits (keeps the JSON line short)."""
+    return None if x is None else float("%.4g" % x)
+
+
+def headline_config():
+    """The configuration both arms report (identical dicts)."""
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[HEADLINE]
+    return {"workload": HEADLINE, "shape": [w.B, w.H, w.T, w.D], "t_cap": w.t_cap, "k_bits": w.k_bits,
+            "k_signed": w.k_signed, "v_bits": HEADLINE_V_BITS, "in_dtype": "bf16", "out_dtype": "bf16",
+            "step": "encode of the whole cache, then its decode (one launch each)",
+            "l2": "inputs larger than L2: 1.07 GB of K, V in and out per launch"}
 
 
 # ---- multi-rank plumbing (host logic; tested with gloo on CPU) --------------------
@@ -108,15 +131,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def profiled_traffic(key: str):
+    """dram bytes per launch ("<kernel>@<workload>") from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(kernel)
+    e = d.get(key)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
@@ -170,37 +193,62 @@ class ClockSampler:
 
 
 # ---- CPU baseline (the oracle) ------------------------------------------------------
-def oracle_timing(rows_target: int, min_seconds: float, max_seconds: float):
+def oracle_timing(rows_target: int, min_seconds: float, max_seconds: float, workload: str = HEADLINE,
+                  v_bits: int = HEADLINE_V_BITS):
     """Time the oracle's encode + decode on row chunks of the workload until
     min_seconds have passed; returns (rows, seconds)."""
-    import numpy as np
-
     import oracle
     from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv, to_oracle
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[workload]
     chunk_T = 256
-    k, v = make_kv(w, T=chunk_T)  # [1, 8, 256, 128]: 2048 rows per chunk
+    k, v = make_kv(w, B=1, T=chunk_T)  # [1, H, 256, D]: 2048 rows per chunk at H = 8
     ko, vo = to_oracle(k), to_oracle(v)
     oracle.lib()
     done, t0 = 0, time.perf_counter()
     while True:
-        cache = oracle.encode_kv(ko, vo, w.k_bits, w.k_signed, w.v_bits[0])
-        oracle.decode_kv(cache, chunk_T, w.k_bits, w.k_signed, w.v_bits[0], out_dtype=oracle.BF16)
+        cache = oracle.encode_kv(ko, vo, w.k_bits, w.k_signed, v_bits)
+        oracle.decode_kv(cache, chunk_T, w.k_bits, w.k_signed, v_bits, out_dtype=oracle.BF16)
         done += ko.shape[1] * chunk_T
         el = time.perf_counter() - t0
         if (el >= min_seconds and done >= min(rows_target, 2048)) or el >= max_seconds:
             return done, el
 
 
+def _oracle_worker(seconds: float):
+    return oracle_timing(2048, seconds, 3 * seconds)
+
+
+def oracle_all_cores(seconds: float):
+    """The same oracle, one process per host core (spawned: no GPU state is
+    inherited), each timing its own chunks; rows/s summed. A timing baseline
+    only: parity uses the single-threaded oracle."""
+    import multiprocessing as mp
+
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [seconds] * n)
+    return sum(r / s for r, s in res), n
+
+
+def cpu_baseline_obj(rows_per_s: float, H: int, sample: str, all_cores=None):
+    d = {"value": r4(rows_per_s / H), "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+         "kind": "oracle", "sample": sample}
+    if all_cores is not None:
+        d["all_cores"] = {"value": r4(all_cores[0] / H), "cores": all_cores[1],
+                          "note": "one oracle process per host core, rows/s summed"}
+    return d
+
+
 def run_reference(args):
-    """The reference arm: the oracle, timed as it stands on the host cores."""
+    """The reference arm: the oracle, timed as it stands on the host cores,
+    on the headline configuration."""
     rank, ws, _ = dist_env()
     if rank != 0:
         return
     from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[HEADLINE]
     per_step_budget = max(0.02, 150.0 / max(1, args.steps + args.warmup))
     # calibrate: rows the oracle encodes + decodes per second
     rows, secs = oracle_timing(2048, 0.5, 5.0)
@@ -213,24 +261,43 @@ def run_reference(args):
         r, s = oracle_timing(step_rows, per_step_budget, per_step_budget * 4)
         total_rows += r
         total_s += s
-    tokens = total_rows / w.H
-    value = tokens / total_s
+    value = total_rows / w.H / total_s
     per_step = total_rows // max(1, args.steps)
-    sample = ("%d rows (%d tokens) of %s per step on average, encode+decode, bf16 out, single-threaded"
-              % (per_step, per_step // w.H, WORKLOAD))
+    sample = ("%d rows (%d tokens) of %s per step on average, encode+decode at %d-bit values, bf16 out, "
+              "single-threaded; tokens/s of that sample" % (per_step, per_step // w.H, HEADLINE, HEADLINE_V_BITS))
+    cpu = cpu_baseline_obj(total_rows / total_s, w.H, sample)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps),
+        "impl": "reference", "metric": METRIC, "value": r4(value), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r4(1e3 * total_s / max(1, args.steps)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "shape": [w.B, w.H, w.T, w.D], "k_bits": 8, "k_signed": True,
-                   "v_bits": 3, "in_dtype": "bf16", "out_dtype": "bf16"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": headline_config(), "cpu_baseline": cpu,
+        "e2e": {"value": r4(value), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ---- the GPU arm --------------------------------------------------------------------
+def roofline_obj(kernel: str, workload: str, bytes_per_launch: int, launch_us: float, peak: float, peak_kind: str):
+    achieved = bytes_per_launch / (launch_us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": r4(achieved), "peak": peak, "unit": "GB/s", "frac": r4(achieved / peak),
+            "traffic": profiled_traffic("%s@%s" % (kernel, workload)), "kernel": kernel, "peak_source": peak_kind,
+            "bytes_per_launch": bytes_per_launch, "launch_us": r4(launch_us)}
+
+
+def codec_roofline(workload: str, vb: int, rows: int, D: int, kb: int, enc_us: float, dec_us: float, peak,
+                   peak_kind):
+    """Roofline object of the slower of a workload's encode and decode
+    launches, plus both launch times."""
+    bpl = rows * bytes_per_row(D, kb, vb, 2)
+    name = "%s_v%d" % (workload, vb)
+    kernel, us = ("encode_kernel", enc_us) if enc_us >= dec_us else ("decode_kernel", dec_us)
+    r = roofline_obj(kernel, name, bpl, us, peak, peak_kind)
+    r["encode_us"], r["decode_us"] = r4(enc_us), r4(dec_us)
+    r["encode_frac"] = r4(bpl / (enc_us * 1e-6) / 1e9 / peak)
+    r["decode_frac"] = r4(bpl / (dec_us * 1e-6) / 1e9 / peak)
+    return r
+
+
 def run_ours(args):
     import turboquant_kv_cache_tq_gb300 as tq
     from turboquant_kv_cache_tq_gb300 import build as tq_build
@@ -246,8 +313,154 @@ def run_ours(args):
         tq_build.build()
     barrier()
     tq.lib()
+    peak, peak_kind = measured_hbm_peak()
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[HEADLINE]
+    kb, ks, vb = w.k_bits, w.k_signed, HEADLINE_V_BITS
+    B, H, T, D, t_cap = w.B, w.H, w.T, w.D, w.t_cap
+    k, v = make_kv(w, device=dev, seed=w.seed + 1000 * rank)
+    cache = tq.alloc_cache(B, H, t_cap, D, kb, vb, device=dev)
+    ko, vo = torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.Stream(device=dev)
+
+    def enc():
+        tq.tq_encode_kv(k, v, kb, ks, vb, cache, stream=stream)
+
+    def dec():
+        tq.tq_decode_kv(cache, T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=ko, v_out=vo, stream=stream)
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            enc()
+            dec()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            for e in ev:
+                e[0].record(stream)
+                enc()
+                e[1].record(stream)
+                dec()
+                e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    enc_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    dec_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    total_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][2]), dev)
+    clocks = clk.summary()
+    value = B * T * args.steps * ws / (total_ms / 1e3)
+    roofline = codec_roofline(HEADLINE, vb, w.rows, D, kb, enc_us, dec_us, peak, peak_kind)
+
+    # ---- e2e through the Python API with pinned host buffers
+    units = [dict(k=k[b:b + E2E_CHUNK], v=v[b:b + E2E_CHUNK], ko=ko[b:b + E2E_CHUNK], vo=vo[b:b + E2E_CHUNK],
+                  cache={n: t[b:b + E2E_CHUNK] for n, t in cache.items()}) for b in range(0, B, E2E_CHUNK)]
+    e2e = run_e2e(args, tq, units, kb, ks, vb, T, dev, stream)
+    e2e_ms = max_over_ranks(e2e["ms"], dev)
+    e2e_value = B * T * e2e["steps"] * ws / (e2e_ms / 1e3)
+    del units, k, v, ko, vo, cache
+    torch.cuda.empty_cache()
+
+    secondary = run_secondary(args, tq, dev, stream, peak, peak_kind, rank) if args.workloads else None
+
+    cpu = None
+    if rank == 0 and ws == 1:
+        rows_done, secs = oracle_timing(w.rows, args.cpu_seconds, 3 * args.cpu_seconds)
+        allc = oracle_all_cores(min(args.cpu_seconds, 5.0)) if args.cpu_all_cores else None
+        cpu = cpu_baseline_obj(rows_done / secs, H,
+                               "%d rows (%d tokens) of %s, encode+decode at %d-bit values, bf16 out, "
+                               "single-threaded; tokens/s of that sample" % (rows_done, rows_done // H, HEADLINE, vb),
+                               allc)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": r4(value), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r4(total_ms / args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": headline_config(),
+            "roofline": roofline,
+            "e2e": {"value": r4(e2e_value), "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
+                    "d2h_bytes_per_step": e2e["d2h"]},
+            "cpu_baseline": cpu,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "secondary": secondary,
+        }
+        print(json.dumps(line, separators=(",", ":")), flush=True)
+    barrier()
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+def _time_launches(fn, stream, reps):
+    """Average ms of fn() (one launch) over reps back-to-back launches, events on `stream`."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        fn()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_secondary(args, tq, dev, stream, peak, peak_kind, rank):
+    """The other configurations, each with its own roofline object."""
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_append_steps, make_kv
+
+    out = {}
+    out["llama3_8b_layer_v3"] = time_layers(tq, dev, stream, peak, peak_kind, rank)
+    for name in ("long_context", "hd256", "hd512"):
+        w = WORKLOADS[name]
+        k, v = make_kv(w, device=dev)
+        ko, vo = torch.empty_like(k), torch.empty_like(v)
+        t_cap = w.t_cap or w.T
+        for vb in w.v_bits:
+            cache = tq.alloc_cache(w.B, w.H, t_cap, w.D, w.k_bits, vb, device=dev)
+            enc = _time_launches(lambda: tq.tq_encode_kv(k, v, w.k_bits, w.k_signed, vb, cache, stream=stream),
+                                 stream, 10)
+            dec = _time_launches(lambda: tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo,
+                                                         stream=stream), stream, 10)
+            key = "%s_v%d" % (name, vb)
+            if not (name == HEADLINE and vb == HEADLINE_V_BITS):
+                out[key] = codec_roofline(name, vb, w.rows, w.D, w.k_bits, 1e3 * enc, 1e3 * dec, peak, peak_kind)
+            if name == "long_context":
+                # decode-step appends: one token per sequence at t_off = T + s (latency-bound)
+                steps = [(a.to(dev), b.to(dev)) for a, b in make_append_steps(w)]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    for s_, (a, b) in enumerate(steps):
+                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
+                torch.cuda.synchronize(dev)
+                with torch.cuda.graph(g, stream=stream):
+                    for s_, (a, b) in enumerate(steps):
+                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
+                ms = _time_launches(g.replay, stream, 20)
+                out["append_v%d" % vb] = {"us_per_step": r4(1e3 * ms / len(steps)), "rows_per_step": w.B * w.H,
+                                          "steps_per_graph": len(steps)}
+                out["attention_v%d" % vb] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, peak_kind)
+                if vb == 3:
+                    out["batched_merge_v3"] = time_merge(tq, w, cache, t_cap, dev, stream, peak)
+            del cache
+        del k, v, ko, vo
+        torch.cuda.empty_cache()
+    out["lloyd_max_fit"] = time_lloyd(tq, dev, stream)
+    return out
+
+
+def time_layers(tq, dev, stream, peak, peak_kind, rank):
+    """The Llama-3-8B-shaped model: encode then decode of all 32 layers' KV
+    for one 4096-token sequence, every layer with its own inputs, cache and
+    outputs (1.28 GB, ten times the L2), as two CUDA graphs of 32 launches;
+    CUDA events around each graph give the per-launch times."""
+    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_kv
+
+    w = WORKLOADS["llama3_8b_layer"]
     kb, ks, vb = w.k_bits, w.k_signed, w.v_bits[0]
     B, H, T, D = w.B, w.H, w.T, w.D
     layers = []
@@ -255,7 +468,6 @@ def run_ours(args):
         k, v = make_kv(w, device=dev, seed=1000 * (rank + 1) + i)
         layers.append(dict(k=k, v=v, cache=tq.alloc_cache(B, H, T, D, kb, vb, device=dev),
                            ko=torch.empty_like(k), vo=torch.empty_like(v)))
-    stream = torch.cuda.Stream(device=dev)
 
     def enc_all():
         for L in layers:
@@ -276,158 +488,31 @@ def run_ours(args):
         enc_all()
     with torch.cuda.graph(g_dec, stream=stream):
         dec_all()
-    torch.cuda.synchronize(dev)
-
+    reps = 50
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(5):
             g_enc.replay()
             g_dec.replay()
+        for e in ev:
+            e[0].record(stream)
+            g_enc.replay()
+            e[1].record(stream)
+            g_dec.replay()
+            e[2].record(stream)
     torch.cuda.synchronize(dev)
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            for e in ev:
-                e[0].record(stream)
-                g_enc.replay()
-                e[1].record(stream)
-                g_dec.replay()
-                e[2].record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-    enc_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    clocks = clk.summary()
-    total_ms = max_over_ranks(total_ms, dev)
-
-    tokens_per_step = B * T * LAYERS
-    value = tokens_per_step * args.steps * ws / (total_ms / 1e3)
-    rows = B * H * T
-    bpl = rows * bytes_per_row(D, kb, vb, 2)
-    enc_launch_us = 1e3 * enc_ms / (args.steps * LAYERS)
-    dec_launch_us = 1e3 * dec_ms / (args.steps * LAYERS)
-    dominant = "encode" if enc_ms >= dec_ms else "decode"
-    launch_us = max(enc_launch_us, dec_launch_us)
-    peak, peak_kind = measured_hbm_peak()
-    achieved = bpl / (launch_us * 1e-6) / 1e9
-    kernel_name = "encode_kernel" if dominant == "encode" else "decode_kernel"
-
-    # ---- e2e through the Python API with pinned host buffers
-    e2e = run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream)
-    e2e_ms = max_over_ranks(e2e["ms"], dev)
-    e2e_value = tokens_per_step * e2e["steps"] * ws / (e2e_ms / 1e3)
-
-    workloads = run_other_workloads(tq, dev, stream, peak) if args.workloads else None
-    if workloads is not None:
-        workloads["lloyd_max_fit"] = time_lloyd(tq, dev, stream, peak)
-
-    cpu = None
-    if rank == 0 and ws == 1:
-        rows_done, secs = oracle_timing(rows, args.cpu_seconds, 3 * args.cpu_seconds)
-        cpu = {"value": rows_done / H / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": "%d rows (%d tokens) of %s, encode+decode, bf16 out, single-threaded"
-                         % (rows_done, rows_done // H, WORKLOAD)}
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers_per_step": LAYERS, "shape": [B, H, T, D],
-                       "k_bits": kb, "k_signed": ks, "v_bits": vb, "in_dtype": "bf16", "out_dtype": "bf16",
-                       "l2": "inputs larger than L2: every layer has its own inputs, cache and outputs "
-                             "(%.2f GB)" % (LAYERS * (4 * rows * D * 2 + rows * (bpl // rows - 4 * D)) / 1e9),
-                       "timing": "CUDA graphs of the 32 encode and 32 decode launches, CUDA events"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(kernel_name),
-                         "kernel": kernel_name, "peak_source": peak_kind,
-                         "bytes_per_launch": bpl, "launch_us": launch_us},
-            "kernels": {"encode_us_per_launch": enc_launch_us, "decode_us_per_launch": dec_launch_us,
-                        "encode_GBps": bpl / (enc_launch_us * 1e-6) / 1e9,
-                        "decode_GBps": bpl / (dec_launch_us * 1e-6) / 1e9},
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
-                    "d2h_bytes_per_step": e2e["d2h"]},
-            "cpu_baseline": cpu,
-            "workloads": workloads,
-            "gpu_launches": 2 * LAYERS * args.steps,
-            "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    barrier()
-    if torch.distributed.is_initialized():
-        torch.distributed.destroy_process_group()
+    enc_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / (reps * LAYERS)
+    dec_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / (reps * LAYERS)
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / reps
+    r = codec_roofline("llama3_8b_layer", vb, w.rows, D, kb, enc_us, dec_us, peak, peak_kind)
+    r["tokens_per_s"] = r4(B * T * LAYERS / (step_ms / 1e3))
+    r["layers_per_step"] = LAYERS
+    del layers, g_enc, g_dec
+    torch.cuda.empty_cache()
+    return r
 
 
-def _time_launches(fn, stream, reps):
-    """Average ms of fn() (one launch) over reps back-to-back launches, events on `stream`."""
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        fn()
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / reps
-
-
-def run_other_workloads(tq, dev, stream, peak):
-    """The other benchmark workloads, one launch at a time (inputs far larger
-    than L2): encode and decode GB/s (algorithmic bytes) and fraction of the
-    HBM peak, plus the long-context decode-step append latency."""
-    from turboquant_kv_cache_tq_gb300.workloads import WORKLOADS, make_append_steps, make_kv
-
-    out = {}
-    for name in ("long_context", "hd256", "hd512"):
-        w = WORKLOADS[name]
-        k, v = make_kv(w, device=dev)
-        ko, vo = torch.empty_like(k), torch.empty_like(v)
-        rows = w.rows
-        for vb in w.v_bits:
-            t_cap = w.t_cap or w.T
-            cache = tq.alloc_cache(w.B, w.H, t_cap, w.D, w.k_bits, vb, device=dev)
-            bpl = rows * bytes_per_row(w.D, w.k_bits, vb, 2)
-            enc = _time_launches(lambda: tq.tq_encode_kv(k, v, w.k_bits, w.k_signed, vb, cache, stream=stream),
-                                 stream, 10)
-            dec = _time_launches(lambda: tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo,
-                                                         stream=stream), stream, 10)
-            r = {"shape": [w.B, w.H, w.T, w.D], "k_bits": w.k_bits, "v_bits": vb, "bytes_per_launch": bpl,
-                 "encode_us": 1e3 * enc, "decode_us": 1e3 * dec,
-                 "encode_GBps": bpl / (enc * 1e-3) / 1e9, "decode_GBps": bpl / (dec * 1e-3) / 1e9,
-                 "encode_tokens_per_s": w.tokens / (enc * 1e-3), "decode_tokens_per_s": w.tokens / (dec * 1e-3)}
-            r["encode_frac"] = r["encode_GBps"] / peak
-            r["decode_frac"] = r["decode_GBps"] / peak
-            if name == "long_context":
-                # decode-step appends: one token per sequence at t_off = T + s
-                steps = [(a.to(dev), b.to(dev)) for a, b in make_append_steps(w)]
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.stream(stream):
-                    for s_, (a, b) in enumerate(steps):
-                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
-                torch.cuda.synchronize(dev)
-                with torch.cuda.graph(g, stream=stream):
-                    for s_, (a, b) in enumerate(steps):
-                        tq.tq_encode_kv(a, b, w.k_bits, w.k_signed, vb, cache, t_off=w.T + s_, stream=stream)
-                ms = _time_launches(g.replay, stream, 20)
-                r["append_us_per_step"] = 1e3 * ms / len(steps)
-                r["append_rows_per_step"] = w.B * w.H
-                # the full cache after the appends decodes like the rest
-                dec_all = _time_launches(lambda: tq.tq_decode_kv(cache, t_cap, w.k_bits, w.k_signed, vb,
-                                                                 stream=stream), stream, 3)
-                r["decode_full_cache_us"] = 1e3 * dec_all
-                r["attention"] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak)
-                r["batched_merge"] = time_merge(tq, w, cache, t_cap, dev, stream, peak)
-            out["%s_v%d" % (name, vb)] = r
-            del cache
-        del k, v, ko, vo
-        torch.cuda.empty_cache()
-    return out
-
-
-def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, G=4):
+def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, peak_kind, G=4):
     """One decode step of fused attention over the whole packed cache (all
     t_cap tokens valid): Llama-3-8B's 4 query heads per kv head, one query
     token per sequence. Algorithmic bytes: the packed cache, read once."""
@@ -440,11 +525,11 @@ def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, G=4):
                                                        workspace=work, stream=stream), stream, 10)
     rows = w.B * w.H * t_cap
     per_row = w.D * w.k_bits // 8 + w.D * vb // 8 + 3 * (w.D // 32) * 2
-    nbytes = rows * per_row
-    return {"query_heads": w.H * G, "query_tokens": 1, "kv_tokens": t_cap, "us": 1e3 * ms,
-            "bytes_per_launch": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9,
-            "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "kv_tokens_per_s": w.B * t_cap / (ms * 1e-3),
-            "workspace_bytes": ws_bytes, "launches": 2}
+    r = roofline_obj("attn_split_kernel", "long_context_attention_v%d" % vb, rows * per_row, 1e3 * ms, peak,
+                     peak_kind)
+    r["kv_tokens_per_s"] = r4(w.B * t_cap / (ms * 1e-3))
+    r["query_heads"], r["kv_tokens"], r["launches"] = w.H * G, t_cap, 2
+    return r
 
 
 def time_merge(tq, w, cache, t_cap, dev, stream, peak):
@@ -460,42 +545,42 @@ def time_merge(tq, w, cache, t_cap, dev, stream, peak):
     ms = _time_launches(lambda: tq.tq_cache_assemble(srcs, dst, width, stream=stream), stream, 10)
     per_tok = sum(t.shape[-1] * t.element_size() for t in cache.values()) * w.H
     nbytes = per_tok * (sum(lens) + B * width)
-    return {"rows": B, "width": width, "us": 1e3 * ms, "bytes_per_launch": nbytes,
-            "GBps": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / peak}
+    return {"us": r4(1e3 * ms), "bytes_per_launch": nbytes, "GBps": r4(nbytes / (ms * 1e-3) / 1e9),
+            "frac": r4(nbytes / (ms * 1e-3) / 1e9 / peak)}
 
 
-def time_lloyd(tq, dev, stream, peak, n=1 << 20, iters=500):
+def time_lloyd(tq, dev, stream, n=1 << 20, iters=500):
     """Lloyd-Max table fit (turboquant-tables.ts: 500 iterations on a
-    unit-normal sample) of 2^20 samples at 4 and 8 bits; bytes per
-    iteration = the sample, read once."""
+    unit-normal sample) of 2^20 samples at 4 and 8 bits, in microseconds per
+    iteration: the 4 MB sample stays in L2 and every iteration is a chain of
+    dependent steps ending in a grid barrier, so HBM bandwidth is not its
+    bound."""
     g = torch.Generator(device=dev).manual_seed(7)
     x = torch.randn(n, generator=g, device=dev)
-    out = {}
+    out = {"samples": n, "iterations": iters}
     for bits in (4, 8):
         K = 1 << bits
         init = torch.linspace(-3.0, 3.0, K, device=dev)
         work = torch.empty(tq.lib().tq_lloyd_max_fit_workspace_size(K), dtype=torch.uint8, device=dev)
         ms = _time_launches(lambda: tq.tq_lloyd_max_fit(x, init, iters, workspace=work, stream=stream), stream, 3)
-        us_it = 1e3 * ms / iters
-        out["bits%d" % bits] = {"samples": n, "iterations": iters, "ms_per_fit": ms, "us_per_iteration": us_it,
-                                "GBps": 4 * n / (us_it * 1e-6) / 1e9, "frac": 4 * n / (us_it * 1e-6) / 1e9 / peak}
+        out["bits%d_us_per_iteration" % bits] = r4(1e3 * ms / iters)
     return out
 
 
-def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
+def run_e2e(args, tq, units, kb, ks, vb, T, dev, stream):
     """Host buffers in, host buffers out, through the Python API. Every step
-    copies each layer's K, V from pinned host memory, encodes and decodes it,
-    and copies the decoded K, V back; layers are pipelined over three streams
-    (uploads, kernels, downloads) with per-layer events, so one layer's copies
-    overlap other layers' kernels and the two copy directions overlap each
+    copies each unit's K, V from pinned host memory, encodes and decodes it,
+    and copies the decoded K, V back; units are pipelined over three streams
+    (uploads, kernels, downloads) with per-unit events, so one unit's copies
+    overlap other units' kernels and the two copy directions overlap each
     other. A device buffer is rewritten only after its previous reader is done
-    (the next step's upload waits for the layer's encode, its decode for the
-    layer's previous download)."""
-    host_in = [(L["k"].cpu().pin_memory(), L["v"].cpu().pin_memory()) for L in layers]
+    (the next step's upload waits for the unit's encode, its decode for the
+    unit's previous download)."""
+    host_in = [(u["k"].cpu().pin_memory(), u["v"].cpu().pin_memory()) for u in units]
     host_out = [(torch.empty_like(a).pin_memory(), torch.empty_like(b).pin_memory()) for a, b in host_in]
     steps = max(1, min(args.steps, args.e2e_steps))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = len(layers)
+    n = len(units)
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_enc = [torch.cuda.Event() for _ in range(n)]
     ev_dec = [torch.cuda.Event() for _ in range(n)]
@@ -503,25 +588,25 @@ def run_e2e(args, tq, layers, kb, ks, vb, T, dev, stream):
     started = [False]
 
     def step():
-        for i, (L, (hk, hv), (ok, ov)) in enumerate(zip(layers, host_in, host_out)):
+        for i, (u, (hk, hv), (ok, ov)) in enumerate(zip(units, host_in, host_out)):
             with torch.cuda.stream(s_in):
                 if started[0]:
                     s_in.wait_event(ev_enc[i])  # the previous step's encode has read the inputs
-                L["k"].copy_(hk, non_blocking=True)
-                L["v"].copy_(hv, non_blocking=True)
+                u["k"].copy_(hk, non_blocking=True)
+                u["v"].copy_(hv, non_blocking=True)
                 ev_in[i].record(s_in)
             stream.wait_event(ev_in[i])
-            tq.tq_encode_kv(L["k"], L["v"], kb, ks, vb, L["cache"], stream=stream)
+            tq.tq_encode_kv(u["k"], u["v"], kb, ks, vb, u["cache"], stream=stream)
             ev_enc[i].record(stream)
             if started[0]:
                 stream.wait_event(ev_out[i])  # the previous step's download has read the outputs
-            tq.tq_decode_kv(L["cache"], T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=L["ko"], v_out=L["vo"],
+            tq.tq_decode_kv(u["cache"], T, kb, ks, vb, out_dtype=torch.bfloat16, k_out=u["ko"], v_out=u["vo"],
                             stream=stream)
             ev_dec[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_dec[i])
-                ok.copy_(L["ko"], non_blocking=True)
-                ov.copy_(L["vo"], non_blocking=True)
+                ok.copy_(u["ko"], non_blocking=True)
+                ov.copy_(u["vo"], non_blocking=True)
                 ev_out[i].record(s_out)
         started[0] = True
 
@@ -622,7 +707,7 @@ def host_link_floor(dev, reps: int):
         print("host link, %s: %.2f ms per 32 layers, %.0f GB/s per direction" % (what, ms, total / ms / 1e6))
 
 
-def run_case(name: str, reps: int):
+def run_case(name: str, reps: int, v_bits=None):
     """A small fixed case for profiling one kernel with ncu: the codec on one
     workload (encode then decode, `reps` times), one fused decode-attention
     step over the long-context cache shape, or the plain-copy floor of the
@@ -662,8 +747,8 @@ def run_case(name: str, reps: int):
         return
     w = WORKLOADS[name]
     k, v = make_kv(w, device=dev)
-    vb = w.v_bits[0]
-    cache = tq.alloc_cache(w.B, w.H, w.T, w.D, w.k_bits, vb, device=dev)
+    vb = w.v_bits[0] if v_bits is None else v_bits
+    cache = tq.alloc_cache(w.B, w.H, w.t_cap or w.T, w.D, w.k_bits, vb, device=dev)
     ko, vo = torch.empty_like(k), torch.empty_like(v)
     torch.cuda.synchronize()
     for r in range(reps):
@@ -682,19 +767,22 @@ def _median_us(events) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
-                    help="skip the secondary long-context / hd256 / hd512 measurements")
+                    help="skip the secondary configurations")
+    ap.add_argument("--no-cpu-all-cores", dest="cpu_all_cores", action="store_false",
+                    help="skip the all-cores oracle timing")
     ap.add_argument("--case", default=None,
                     help="profiling aid: run one small case (a workload name, 'attention', 'copy_floor' or 'host_link') --reps times")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--v-bits", type=int, default=None, help="value bits of a --case workload")
     args = ap.parse_args(argv)
     if args.case:
-        run_case(args.case, args.reps)
+        run_case(args.case, args.reps, args.v_bits)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
