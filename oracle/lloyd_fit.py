@@ -13,16 +13,22 @@ centroids nor the handling of an empty cell; the readings taken here:
   - one iteration: boundaries are the fp32 midpoints of adjacent centroids,
     RN(c_k + c_{k+1}) / 2 (the printed tables' boundaries are those
     midpoints); each sample goes to cell count(boundaries < x), the codec's
-    searchsorted; each centroid becomes the mean of its cell's samples, the
-    sum and the division in float64 and the quotient rounded to fp32 once;
-    a cell with no samples keeps its centroid;
+    searchsorted; each centroid becomes the mean of its cell's samples: the
+    exact sum over the exact count, rounded once to fp32 (round to nearest,
+    ties to even); a cell with no samples keeps its centroid;
   - the result is the centroids after the last iteration and their
     midpoints.
-Library steps used: numpy's searchsorted (side="left" counts the boundaries
-strictly below x) and bincount (per-cell counts and float64 sums, added in
-sample order).
+Exact sums: every sample is an integer multiple of 2^-64 when it is 0 or
+|x| >= 2^-41 (an fp32 value's last bit is then worth at least 2^-64), so each
+sample splits into integer parts of 2^-32 and 2^-64 units and the cell sums
+are integer sums; samples outside that range (or with |x| >= 2^8) are
+refused. Library steps used: numpy's searchsorted (side="left" counts the
+boundaries strictly below x) and bincount (per-cell counts, and per-cell sums
+of integer pieces below 2^21, which float64 adds exactly).
 """
 from __future__ import annotations
+
+from fractions import Fraction
 
 import numpy as np
 
@@ -32,15 +38,76 @@ def midpoints(c: np.ndarray) -> np.ndarray:
     return ((c[:-1] + c[1:]).astype(np.float32) * np.float32(0.5)).astype(np.float32)
 
 
+def cells(x: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """Cell of every sample: count(boundaries < x)."""
+    return np.searchsorted(midpoints(c), x, side="left")
+
+
+def _check_domain(x: np.ndarray) -> None:
+    a = np.abs(x.astype(np.float64))
+    if not np.all(np.isfinite(a)) or np.any(a >= 256.0) or np.any((a > 0) & (a < 2.0 ** -41)):
+        raise ValueError("lloyd oracle: samples must be 0 or 2^-41 <= |x| < 2^8 (exact in 2^-64 units)")
+
+
+def _bincount_exact(idx: np.ndarray, v: np.ndarray, K: int) -> list[int]:
+    """Per-cell sums of the non-negative int64 values v < 2^41, as Python ints:
+    two pieces below 2^21 each, summed by bincount in float64 (exact: every
+    partial sum of at most 2^31 pieces stays below 2^52)."""
+    hi = (v >> 20).astype(np.float64)
+    lo = (v & ((1 << 20) - 1)).astype(np.float64)
+    sh = np.bincount(idx, weights=hi, minlength=K)
+    sl = np.bincount(idx, weights=lo, minlength=K)
+    return [(int(a) << 20) + int(b) for a, b in zip(sh, sl)]
+
+
+def cell_sums(x: np.ndarray, idx: np.ndarray, K: int) -> list[Fraction]:
+    """Exact per-cell sums of the fp32 samples x (cell idx), as Fractions."""
+    x64 = np.asarray(x, np.float32).astype(np.float64)
+    if x64.size > (1 << 31):
+        raise ValueError("lloyd oracle: at most 2^31 samples")
+    t = x64 * 2.0 ** 32  # exact (a power-of-two scaling)
+    whole = np.floor(t)  # multiples of 2^-32 (|x| < 2^8: |whole| < 2^40)
+    frac = (t - whole) * 2.0 ** 32  # exact: the integer count of 2^-64 units left, in [0, 2^32)
+    w = whole.astype(np.int64) + (1 << 40)  # made non-negative for the split
+    f = frac.astype(np.int64)
+    sw = _bincount_exact(idx, w, K)
+    sf = _bincount_exact(idx, f, K)
+    cnt = np.bincount(idx, minlength=K)
+    return [Fraction(((sw[k] - int(cnt[k]) * (1 << 40)) << 32) + sf[k], 1 << 64) for k in range(K)]
+
+
+def round_f32(q: Fraction) -> np.float32:
+    """The fp32 value nearest to the rational q (ties to even), |q| < 2^128."""
+    if q == 0:
+        return np.float32(0.0)
+    s = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()  # 2^e <= a < 2^(e+2)
+    if Fraction(2) ** e > a:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126)  # below the normal range the last bit is worth 2^-149
+    scaled = a * Fraction(2) ** (23 - e)  # the 24-bit significand, with a fraction
+    m, r = divmod(scaled.numerator, scaled.denominator)
+    twice = 2 * r
+    if twice > scaled.denominator or (twice == scaled.denominator and (m & 1)):
+        m += 1
+    return np.float32(s * float(m) * 2.0 ** (e - 23))  # exact: m <= 2^24
+
+
 def lloyd_step(x: np.ndarray, c: np.ndarray) -> np.ndarray:
     """One Lloyd iteration: the new centroids."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    _check_domain(x)
     K = c.shape[0]
-    idx = np.searchsorted(midpoints(c), x, side="left")
+    idx = cells(x, c)
     cnt = np.bincount(idx, minlength=K)
-    s = np.bincount(idx, weights=x.astype(np.float64), minlength=K)
-    out = c.copy()
-    nz = cnt > 0
-    out[nz] = (s[nz] / cnt[nz]).astype(np.float32)
+    sums = cell_sums(x, idx, K)
+    out = np.array(c, np.float32).copy()
+    for k in range(K):
+        if cnt[k] > 0:
+            out[k] = round_f32(sums[k] / int(cnt[k]))
     return out
 
 
@@ -57,6 +124,6 @@ def lloyd_max_fit(x, init, iters: int):
 def distortion(x, c) -> float:
     """Mean squared error of quantising x to the centroids c (float64)."""
     x = np.asarray(x, np.float32)
-    idx = np.searchsorted(midpoints(c), x, side="left")
+    idx = cells(x, c)
     d = x.astype(np.float64) - np.asarray(c, np.float64)[idx]
     return float(np.mean(d * d))

@@ -86,3 +86,54 @@ def test_distortion_never_increases():
         assert d2 <= d * (1 + 1e-12)
         d = d2
     assert np.all(np.diff(c) > 0)
+
+
+# ---- the exact cell means ---------------------------------------------------------------
+def test_cell_sums_are_the_correctly_rounded_sums():
+    """float() of each exact cell sum equals math.fsum of the cell's samples
+    (Python's fsum returns the correctly rounded sum of its inputs), on
+    samples spanning 2^-40 .. 2^7 in magnitude."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-40, 6, 200000))).astype(np.float32)
+    c = np.linspace(-1.0, 1.0, 8).astype(np.float32)
+    idx = lf.cells(x, c)
+    sums = lf.cell_sums(x, idx, 8)
+    for k in range(8):
+        assert float(sums[k]) == math.fsum(x[idx == k].astype(np.float64).tolist())
+
+
+def test_round_f32_single_rounding_and_ties():
+    from fractions import Fraction
+
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal(20000) * np.exp2(rng.integers(-140, 100, 20000))
+    for d in v:  # a float64 value rounded once to fp32 is numpy's cast
+        assert lf.round_f32(Fraction(float(d))) == np.float32(d)
+    one = Fraction(1)
+    assert lf.round_f32(one + Fraction(1, 1 << 24)) == np.float32(1.0)  # tie -> even
+    assert lf.round_f32(one + Fraction(3, 1 << 24)) == np.float32(1.0 + 2.0 ** -22)
+    assert lf.round_f32(Fraction(1, 1 << 150)) == np.float32(0.0)  # half the smallest subnormal
+    assert lf.round_f32(Fraction(3, 1 << 150)) == np.float32(2.0 ** -148)
+    assert lf.round_f32(-Fraction(5, 3)) == np.float32(-5.0 / 3.0)
+
+
+def test_exact_mean_where_float64_accumulation_is_not():
+    """A cell of 2^16 - 1 samples 255, one 255.5 and 2^16 samples 2^-30: the
+    exact mean is 127.5 + 2^-18 + 2^-31, just above the midpoint between the
+    fp32 neighbours 127.5 and 127.5 + 2^-17, so it rounds up. A float64
+    running sum in sample order loses every 2^-30 (a quarter of its last bit
+    at 2^24) and lands exactly on the midpoint, which rounds to the even
+    127.5: the cell mean must be the exact one."""
+    x = np.concatenate([np.full((1 << 16) - 1, 255.0), [255.5], np.full(1 << 16, 2.0 ** -30)]).astype(np.float32)
+    c = lf.lloyd_step(x, np.array([-100.0, 100.0], np.float32))
+    assert c[0] == np.float32(-100.0)  # empty cell
+    assert c[1] == np.float32(127.5 + 2.0 ** -17)
+    running = np.bincount(np.ones(x.size, np.int64), weights=x.astype(np.float64), minlength=2)[1]
+    assert np.float32(running / x.size) == np.float32(127.5)
+
+
+def test_samples_outside_the_exact_range_are_refused():
+    with pytest.raises(ValueError):
+        lf.lloyd_step(np.array([1.0, 2.0 ** -45], np.float32), np.array([-1.0, 1.0], np.float32))
+    with pytest.raises(ValueError):
+        lf.lloyd_step(np.array([300.0], np.float32), np.array([-1.0, 1.0], np.float32))
