@@ -47,7 +47,8 @@ typedef enum {
                                k_signed with k_bits != 8 */
     TQ_ERR_ALIGNMENT = 4,   /* dim*bits not a multiple of 8; a buffer not 16-byte aligned */
     TQ_ERR_DTYPE = 5,       /* unknown tq_dtype */
-    TQ_ERR_CUDA = 6         /* the CUDA runtime reported an error */
+    TQ_ERR_CUDA = 6,        /* the CUDA runtime reported an error */
+    TQ_ERR_TIMEOUT = 7      /* a bounded device-side wait gave up (tq_lloyd_max_fit_status) */
 } tq_status;
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
@@ -176,7 +177,13 @@ int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, in
  *   - Returns TQ_ERR_INVALID_ARG when the scratch these sizes need,
  *     tq_decode_attention_workspace_size(B, Hkv, T, D), is larger than
  *     TQ_ATTENTION_NOALLOC_SCRATCH_BYTES; every other check and result is
- *     that of tq_decode_attention.
+ *     that of tq_decode_attention (an empty batch, B == 0, returns TQ_OK
+ *     without looking at the scratch). The need is one partial record of
+ *     16 * (D + 2) floats per split block and per (batch, kv head) pair, with
+ *     at most 8 split blocks per SM, so the largest B * Hkv served is
+ *     floor(TQ_ATTENTION_NOALLOC_SCRATCH_BYTES / (64 * (D + 2))) - 8 * SMs:
+ *     on a 152-SM GB300 that is 14671, 6849 and 2848 pairs at head_dim 64,
+ *     128 and 256, independent of the number of tokens.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture. TQ_ERR_CUDA if the lookup fails.
@@ -184,7 +191,7 @@ int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, in
  *     GPU (streams with no ordering between them) race. Order them on one
  *     stream or with events. Nothing in the array needs clearing between
  *     calls: each call writes every scratch record it reads. */
-#define TQ_ATTENTION_NOALLOC_SCRATCH_BYTES (16LL << 20)
+#define TQ_ATTENTION_NOALLOC_SCRATCH_BYTES (64LL << 20)
 tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64_t Hq, int64_t Nq,
                                       const void* k_codes, const void* k_scales, const void* k_zeros,
                                       const void* v_codes, const void* v_scales,
@@ -248,10 +255,32 @@ tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H
  *              bytes (16-byte aligned; the call clears it first).
  * One cooperative kernel runs every iteration (its blocks meet at a bounded
  * grid barrier per iteration; if a wait gives up, centroids and boundaries
- * are left NaN); n < 2^31. */
+ * are left NaN and tq_lloyd_max_fit_status reports TQ_ERR_TIMEOUT);
+ * n < 2^31. Returns once the work is enqueued. */
 tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
                            float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
                            void* stream);
+
+/* tq_lloyd_max_fit with the grid barrier's give-up made explicit (no
+ * counterpart on the pages: failure detection of this library's
+ * cooperative kernel).
+ *   spin_limit    polls (about 64 ns each) a block waits at a grid barrier
+ *                 before it gives up; 0 takes the default 2^22 (about a
+ *                 quarter of a second). At most 2^32 - 1.
+ *   absent_block  -1, or a test hook: the index of a block that leaves the
+ *                 kernel at its first barrier without arriving, as a block
+ *                 that died would; every other block's wait then runs out,
+ *                 the error word is set and centroids and boundaries are
+ *                 left NaN. Every wait stays bounded either way. */
+tq_status tq_lloyd_max_fit_bounded(const float* x, int64_t n, int levels, int iters, const float* init,
+                                   float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
+                                   int64_t spin_limit, int absent_block, void* stream);
+
+/* Outcome of the last fit enqueued with `workspace`: waits for `stream`,
+ * then reads the fit's error word from the workspace (byte offset 8).
+ * TQ_OK, or TQ_ERR_TIMEOUT when a block gave up at a grid barrier (the
+ * results are then NaN); TQ_ERR_CUDA if the wait or the copy failed. */
+tq_status tq_lloyd_max_fit_status(const void* workspace, void* stream);
 
 /* Bytes of scratch tq_lloyd_max_fit needs (64 + 48 * levels), or
  * -TQ_ERR_INVALID_ARG for a level count that is not a power of two in

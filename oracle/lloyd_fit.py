@@ -60,20 +60,27 @@ def _bincount_exact(idx: np.ndarray, v: np.ndarray, K: int) -> list[int]:
     return [(int(a) << 20) + int(b) for a, b in zip(sh, sl)]
 
 
-def cell_sums(x: np.ndarray, idx: np.ndarray, K: int) -> list[Fraction]:
-    """Exact per-cell sums of the fp32 samples x (cell idx), as Fractions."""
-    x64 = np.asarray(x, np.float32).astype(np.float64)
-    if x64.size > (1 << 31):
+def cell_sums(x: np.ndarray, idx: np.ndarray, K: int, chunk: int = 1 << 24) -> list[Fraction]:
+    """Exact per-cell sums of the fp32 samples x (cell idx), as Fractions
+    (computed in chunks of `chunk` samples to bound the memory)."""
+    x = np.asarray(x, np.float32)
+    if x.size > (1 << 31):
         raise ValueError("lloyd oracle: at most 2^31 samples")
-    t = x64 * 2.0 ** 32  # exact (a power-of-two scaling)
-    whole = np.floor(t)  # multiples of 2^-32 (|x| < 2^8: |whole| < 2^40)
-    frac = (t - whole) * 2.0 ** 32  # exact: the integer count of 2^-64 units left, in [0, 2^32)
-    w = whole.astype(np.int64) + (1 << 40)  # made non-negative for the split
-    f = frac.astype(np.int64)
-    sw = _bincount_exact(idx, w, K)
-    sf = _bincount_exact(idx, f, K)
-    cnt = np.bincount(idx, minlength=K)
-    return [Fraction(((sw[k] - int(cnt[k]) * (1 << 40)) << 32) + sf[k], 1 << 64) for k in range(K)]
+    total = [0] * K  # in units of 2^-64
+    for a in range(0, x.size, chunk):
+        x64 = x[a:a + chunk].astype(np.float64)
+        ix = idx[a:a + chunk]
+        t = x64 * 2.0 ** 32  # exact (a power-of-two scaling)
+        whole = np.floor(t)  # multiples of 2^-32 (|x| < 2^8: |whole| < 2^40)
+        frac = (t - whole) * 2.0 ** 32  # exact: the integer count of 2^-64 units left, in [0, 2^32)
+        w = whole.astype(np.int64) + (1 << 40)  # made non-negative for the split
+        f = frac.astype(np.int64)
+        sw = _bincount_exact(ix, w, K)
+        sf = _bincount_exact(ix, f, K)
+        cnt = np.bincount(ix, minlength=K)
+        for k in range(K):
+            total[k] += ((sw[k] - int(cnt[k]) * (1 << 40)) << 32) + sf[k]
+    return [Fraction(t_, 1 << 64) for t_ in total]
 
 
 def round_f32(q: Fraction) -> np.float32:
@@ -109,6 +116,51 @@ def lloyd_step(x: np.ndarray, c: np.ndarray) -> np.ndarray:
         if cnt[k] > 0:
             out[k] = round_f32(sums[k] / int(cnt[k]))
     return out
+
+
+class SortedSample:
+    """A sample sorted once, with exact prefix sums, so that the exact cell
+    sums and counts of any centroids take a binary search per boundary (a sum
+    does not depend on the order of its terms). Cell k holds the samples with
+    b_{k-1} < x <= b_k, i.e. count(boundaries < x) = k. At most 2^22 samples
+    (the prefix sums stay below 2^62)."""
+
+    def __init__(self, x):
+        xs = np.sort(np.asarray(x, np.float32))
+        _check_domain(xs)
+        if xs.size > (1 << 22):
+            raise ValueError("SortedSample: at most 2^22 samples")
+        t = xs.astype(np.float64) * 2.0 ** 32
+        whole = np.floor(t)
+        frac = (t - whole) * 2.0 ** 32
+        z = np.zeros(1, np.int64)
+        self.xs = xs
+        self.pw = np.concatenate([z, np.cumsum(whole.astype(np.int64))])  # 2^-32 units
+        self.pf = np.concatenate([z, np.cumsum(frac.astype(np.int64))])   # 2^-64 units
+        self.off_grid = np.concatenate([z, np.cumsum((t != np.rint(t)).astype(np.int64))])
+
+    def cells(self, c: np.ndarray):
+        """(start, end) index ranges of every cell in the sorted sample."""
+        cut = np.searchsorted(self.xs, midpoints(c), side="right")
+        edges = np.concatenate([[0], cut, [self.xs.size]])
+        return edges[:-1], edges[1:]
+
+    def sums(self, c: np.ndarray):
+        """Exact cell sums (Fractions), counts and counts of samples that are
+        not multiples of 2^-32."""
+        a, b = self.cells(c)
+        sums = [Fraction((int(self.pw[e] - self.pw[s]) << 32) + int(self.pf[e] - self.pf[s]), 1 << 64)
+                for s, e in zip(a, b)]
+        return sums, (b - a), self.off_grid[b] - self.off_grid[a]
+
+    def step(self, c: np.ndarray) -> np.ndarray:
+        """lloyd_step on this sample."""
+        sums, cnt, _ = self.sums(c)
+        out = np.array(c, np.float32).copy()
+        for k in range(out.shape[0]):
+            if cnt[k] > 0:
+                out[k] = round_f32(sums[k] / int(cnt[k]))
+        return out
 
 
 def lloyd_max_fit(x, init, iters: int):

@@ -12,7 +12,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tq.h")
 
-OK, INVALID, HEAD_DIM, BITS, ALIGN, DTYPE, CUDA = range(7)
+OK, INVALID, HEAD_DIM, BITS, ALIGN, DTYPE, CUDA, TIMEOUT = range(8)
 
 
 @pytest.fixture(scope="module")
@@ -54,7 +54,7 @@ def test_packed_dim(L):
 
 
 def test_status_strings(L):
-    for s in range(7):
+    for s in range(8):
         assert L.tq_status_string(s).startswith(b"TQ_")
     assert b"unknown" in L.tq_status_string(99)
 
@@ -209,3 +209,21 @@ def test_cache_assemble_checks(L):
     assert call([tq.TQRowSource(src[0] + 4, *src[1:], 1, 0, 16, 0, 8)]) == ALIGN
     assert call([ok_row], dst=[d[0] + 8] + d[1:]) == ALIGN
     assert call([ok_row], n=0) == OK and call([ok_row], width=0) == OK
+
+
+def test_lloyd_fit_checks(L):
+    """Host checks of the Lloyd fit entry points (no device work is reached)."""
+    base = 1 << 20
+    x, init, c, b, ws = base, base + 4096, base + 8192, base + 12288, base + 16384
+    need = L.tq_lloyd_max_fit_workspace_size(16)
+    assert need == 64 + 48 * 16
+    assert L.tq_lloyd_max_fit_workspace_size(3) == -INVALID
+    assert L.tq_lloyd_max_fit(x, 100, 3, 1, init, c, b, ws, need, None) == INVALID      # not a power of two
+    assert L.tq_lloyd_max_fit(x, 100, 16, 1, init, c, b, ws, need - 1, None) == INVALID  # workspace too small
+    assert L.tq_lloyd_max_fit(x + 2, 100, 16, 1, init, c, b, ws, need, None) == ALIGN
+    assert L.tq_lloyd_max_fit(x, 100, 16, 1, init, c, b, ws + 4, need, None) == ALIGN
+    assert L.tq_lloyd_max_fit_bounded(x, 100, 16, 1, init, c, b, ws, need, -1, -1, None) == INVALID
+    assert L.tq_lloyd_max_fit_bounded(x, 100, 16, 1, init, c, b, ws, need, 1 << 32, -1, None) == INVALID
+    assert L.tq_lloyd_max_fit_bounded(x, 100, 16, 1, init, c, b, ws, need, 100, -2, None) == INVALID
+    assert L.tq_lloyd_max_fit_status(None, None) == INVALID
+    assert L.tq_lloyd_max_fit_status(ws + 8, None) == ALIGN

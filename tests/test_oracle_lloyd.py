@@ -137,3 +137,24 @@ def test_samples_outside_the_exact_range_are_refused():
         lf.lloyd_step(np.array([1.0, 2.0 ** -45], np.float32), np.array([-1.0, 1.0], np.float32))
     with pytest.raises(ValueError):
         lf.lloyd_step(np.array([300.0], np.float32), np.array([-1.0, 1.0], np.float32))
+
+
+def test_sorted_sample_steps_equal_the_plain_steps():
+    """The prefix-sum form of an iteration (sorted sample) equals the plain
+    per-sample form, cell sums and all, including boundary ties and samples
+    below 2^-9."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(50000)
+    x[:2000] = np.sign(x[:2000]) * np.exp2(rng.uniform(-40, -9, 2000))
+    x = x.astype(np.float32)
+    c = np.linspace(-2.0, 2.0, 16).astype(np.float32)
+    x[2000:2100] = lf.midpoints(c)[3]  # samples exactly on a boundary
+    ss = lf.SortedSample(x)
+    for _ in range(6):
+        sums, cnt, _ = ss.sums(c)
+        idx = lf.cells(x, c)
+        assert np.array_equal(cnt, np.bincount(idx, minlength=16))
+        assert sums == lf.cell_sums(x, idx, 16)
+        c2 = ss.step(c)
+        assert np.array_equal(c2, lf.lloyd_step(x, c))
+        c = c2

@@ -21,6 +21,7 @@ __all__ = [
     "TQError", "lib", "tq_packed_dim", "tq_encode_kv", "tq_decode_kv", "tq_decode_kv_rotated",
     "tq_unrotate", "tq_lloyd_max_index", "tq_decode_attention", "tq_decode_attention_workspace_size",
     "tq_cache_assemble", "merge_rows", "extend_rows", "extract_row", "filter_rows", "tq_lloyd_max_fit",
+    "tq_lloyd_max_fit_status",
     "tq_status_string", "alloc_cache", "HEAD_DIMS", "VALUE_BITS", "KEY_MODES",
 ]
 
@@ -33,7 +34,7 @@ GROUP = 32
 TQ_F32, TQ_BF16 = 0, 1
 _DTYPE = {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16}
 _NAMES = ("TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_ALIGNMENT",
-          "TQ_ERR_DTYPE", "TQ_ERR_CUDA")
+          "TQ_ERR_DTYPE", "TQ_ERR_CUDA", "TQ_ERR_TIMEOUT")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,10 @@ def lib() -> ctypes.CDLL:
             L.tq_cache_assemble.argtypes = [P, I64, I64, I64, I, I, P, P, P, P, P, I64, I64, P]
             L.tq_lloyd_max_fit.restype = I
             L.tq_lloyd_max_fit.argtypes = [P, I64, I, I, P, P, P, P, I64, P]
+            L.tq_lloyd_max_fit_bounded.restype = I
+            L.tq_lloyd_max_fit_bounded.argtypes = [P, I64, I, I, P, P, P, P, I64, I64, I, P]
+            L.tq_lloyd_max_fit_status.restype = I
+            L.tq_lloyd_max_fit_status.argtypes = [P, P]
             L.tq_lloyd_max_fit_workspace_size.restype = I64
             L.tq_lloyd_max_fit_workspace_size.argtypes = [I]
             L.tq_status_string.restype = ctypes.c_char_p
@@ -346,9 +351,12 @@ def filter_rows(batch, S: int, keep, stream=None) -> dict:
 
 
 # ---- Lloyd-Max table fit (turboquant-tables.ts) -----------------------------------
-def tq_lloyd_max_fit(x: torch.Tensor, init: torch.Tensor, iters: int, workspace=None, stream=None):
+def tq_lloyd_max_fit(x: torch.Tensor, init: torch.Tensor, iters: int, workspace=None, stream=None,
+                     spin_limit: int = 0, absent_block: int = -1):
     """Lloyd-Max fit of len(init) levels to the fp32 samples x (device), from
-    the ascending centroids init -> (centroids, boundaries), fp32 tensors."""
+    the ascending centroids init -> (centroids, boundaries), fp32 tensors.
+    spin_limit / absent_block: see tq_lloyd_max_fit_bounded (0 / -1: the
+    plain fit); tq_lloyd_max_fit_status(workspace) reports a give-up."""
     if x.dtype != torch.float32 or init.dtype != torch.float32 or not (x.is_contiguous() and init.is_contiguous()):
         raise ValueError("x and init must be contiguous float32 tensors")
     K = init.numel()
@@ -359,7 +367,17 @@ def tq_lloyd_max_fit(x: torch.Tensor, init: torch.Tensor, iters: int, workspace=
         workspace = torch.empty(r, dtype=torch.uint8, device=x.device)
     c = torch.empty(K, dtype=torch.float32, device=x.device)
     b = torch.empty(max(K - 1, 1), dtype=torch.float32, device=x.device)
-    st = lib().tq_lloyd_max_fit(x.data_ptr(), x.numel(), K, int(iters), init.data_ptr(), c.data_ptr(), b.data_ptr(),
-                                workspace.data_ptr(), workspace.numel(), _stream_handle(stream, x.device))
+    st = lib().tq_lloyd_max_fit_bounded(x.data_ptr(), x.numel(), K, int(iters), init.data_ptr(), c.data_ptr(),
+                                        b.data_ptr(), workspace.data_ptr(), workspace.numel(), int(spin_limit),
+                                        int(absent_block), _stream_handle(stream, x.device))
     _check(st, "tq_lloyd_max_fit")
     return c, b[: K - 1]
+
+
+def tq_lloyd_max_fit_status(workspace: torch.Tensor, stream=None) -> int:
+    """Waits for `stream`, then returns the status of the last fit run with
+    `workspace`: 0 (TQ_OK) or 7 (TQ_ERR_TIMEOUT: a grid-barrier wait gave up)."""
+    st = int(lib().tq_lloyd_max_fit_status(workspace.data_ptr(), _stream_handle(stream, workspace.device)))
+    if st not in (0, 7):
+        raise TQError(st, "tq_lloyd_max_fit_status")
+    return st

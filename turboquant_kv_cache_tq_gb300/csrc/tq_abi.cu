@@ -346,6 +346,7 @@ extern "C" const char* tq_status_string(int status) {
     case TQ_ERR_ALIGNMENT: return "TQ_ERR_ALIGNMENT: size not byte-aligned or buffer not 16-byte aligned";
     case TQ_ERR_DTYPE: return "TQ_ERR_DTYPE: dtype must be TQ_F32 or TQ_BF16";
     case TQ_ERR_CUDA: return "TQ_ERR_CUDA: the CUDA runtime reported an error";
+    case TQ_ERR_TIMEOUT: return "TQ_ERR_TIMEOUT: a bounded device-side wait gave up";
     default: return "unknown tq_status";
   }
 }

@@ -49,6 +49,8 @@ struct LloydParams {
   long long* sums;           // [3][levels], zero on entry
   unsigned long long* cnts;  // [3][levels], zero on entry
   unsigned* bar;             // arrivals, generation, error; zero on entry
+  unsigned spin_limit;       // polls a block waits at a barrier before it gives up
+  int absent_block;          // a block that leaves at its first barrier without arriving, or -1
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -58,10 +60,14 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 }
 
 // Grid barrier of a cooperative launch (all blocks resident). False when the
-// wait gave up or another block reported an error.
-__device__ bool grid_barrier(unsigned* bar) {
+// wait gave up or another block reported an error. A block that gives up
+// sets the error word bar[2] (read by tq_lloyd_max_fit_status). The absent
+// block (failure-detection test hook) returns false without arriving, so
+// every other block's wait runs out after spin_limit polls.
+__device__ bool grid_barrier(unsigned* bar, unsigned spin_limit, int absent_block) {
   __shared__ int s_ok;
   __syncthreads();
+  if (static_cast<int>(blockIdx.x) == absent_block) return false;
   if (threadIdx.x == 0) {
     const unsigned gen = ld_acquire(bar + 1);
     int ok = 1;
@@ -73,7 +79,7 @@ __device__ bool grid_barrier(unsigned* bar) {
     } else {
       unsigned spins = 0;
       while (ld_acquire(bar + 1) == gen) {
-        if (++spins > kLloydSpinLimit) {
+        if (++spins > spin_limit) {
           atomicExch(bar + 2, 1u);
           ok = 0;
           break;
@@ -178,7 +184,8 @@ __global__ void __launch_bounds__(kLloydThreads) lloyd_fit_kernel(LloydParams p)
         atomicAdd(cnts + k, static_cast<unsigned long long>(c));
       }
     }
-    if (!grid_barrier(p.bar)) {
+    if (!grid_barrier(p.bar, p.spin_limit, p.absent_block)) {
+      if (static_cast<int>(blockIdx.x) == p.absent_block) return;
       for (int k = threadIdx.x; k < K; k += blockDim.x) {
         p.centroids[k] = __int_as_float(0x7fc00000);
         if (k < K - 1) p.boundaries[k] = __int_as_float(0x7fc00000);
@@ -234,10 +241,12 @@ extern "C" int64_t tq_lloyd_max_fit_workspace_size(int levels) {
   return 64 + 48LL * levels;  // barrier words, then three buffers of int64 sums and counts per level
 }
 
-extern "C" tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
-                                      float* centroids, float* boundaries, void* workspace,
-                                      int64_t workspace_bytes, void* stream) {
+extern "C" tq_status tq_lloyd_max_fit_bounded(const float* x, int64_t n, int levels, int iters,
+                                              const float* init, float* centroids, float* boundaries,
+                                              void* workspace, int64_t workspace_bytes, int64_t spin_limit,
+                                              int absent_block, void* stream) {
   using namespace tq;
+  if (spin_limit < 0 || spin_limit > 0xffffffffLL || absent_block < -1) return TQ_ERR_INVALID_ARG;
   if (n < 0 || iters < 0 || levels < 2 || levels > 256 || (levels & (levels - 1)) != 0) return TQ_ERR_INVALID_ARG;
   if (n > (1LL << 31) - 1) return TQ_ERR_INVALID_ARG;
   if (!init || !centroids || !boundaries || !workspace || (n > 0 && !x)) return TQ_ERR_INVALID_ARG;
@@ -256,6 +265,8 @@ extern "C" tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int
   p.centroids = centroids;
   p.boundaries = boundaries;
   p.bar = reinterpret_cast<unsigned*>(ws);
+  p.spin_limit = spin_limit == 0 ? kLloydSpinLimit : static_cast<unsigned>(spin_limit);
+  p.absent_block = absent_block;
   p.sums = reinterpret_cast<long long*>(ws + 64);
   p.cnts = reinterpret_cast<unsigned long long*>(ws + 64 + 24LL * levels);
   if (cudaMemcpyAsync(centroids, init, sizeof(float) * levels, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
@@ -276,4 +287,22 @@ extern "C" tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int
       return TQ_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
+                                      float* centroids, float* boundaries, void* workspace,
+                                      int64_t workspace_bytes, void* stream) {
+  return tq_lloyd_max_fit_bounded(x, n, levels, iters, init, centroids, boundaries, workspace, workspace_bytes, 0,
+                                  -1, stream);
+}
+
+extern "C" tq_status tq_lloyd_max_fit_status(const void* workspace, void* stream) {
+  if (!workspace) return TQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return TQ_ERR_ALIGNMENT;
+  unsigned err = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(&err, static_cast<const uint8_t*>(workspace) + 8, sizeof(err), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return TQ_ERR_CUDA;
+  return err != 0 ? TQ_ERR_TIMEOUT : TQ_OK;
 }
