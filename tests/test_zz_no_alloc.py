@@ -26,7 +26,7 @@ import turboquant_kv_cache_tq_gb300 as tq
 pytestmark = pytest.mark.gpu
 
 ATTN_TOL = 5e-6  # the attention parity tolerance (x max|Vrot|), as in test_gpu_attention.py
-SCRATCH_BYTES = 16 << 20  # TQ_ATTENTION_NOALLOC_SCRATCH_BYTES in include/tq.h
+SCRATCH_BYTES = 64 << 20  # TQ_ATTENTION_NOALLOC_SCRATCH_BYTES in include/tq.h
 
 
 @pytest.fixture(scope="module")
@@ -66,7 +66,8 @@ def _vrot_max(cache, T, kb, ks, vb):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(L):
-    cases = [(4, 8, 4, 1000, 128, 8, True, 3, 1), (2, 4, 2, 333, 64, 4, False, 5, 2)]
+    cases = [(4, 8, 4, 1000, 128, 8, True, 3, 1), (2, 4, 2, 333, 64, 4, False, 5, 2),
+             (3, 8, 2, 517, 256, 8, True, 4, 3)]
     for (B, Hkv, G, T, D, kb, ks, vb, seed) in cases:
         q, cache, lp, t_cap = _case(B, Hkv, G, T, D, kb, ks, vb, seed)
         assert tq.tq_decode_attention_workspace_size(B, Hkv, T, D) <= SCRATCH_BYTES
@@ -82,13 +83,25 @@ def test_noalloc_matches_workspace_entry_point_twice(L):
 
 
 def test_noalloc_refuses_sizes_beyond_the_scratch(L):
-    # 64 x 64 (batch, kv head) pairs over 2^20 tokens need far more than the
-    # fixed array; the call is refused on the host, before any launch
-    need = tq.tq_decode_attention_workspace_size(64, 64, 1 << 20, 128)
+    # 128 x 64 (batch, kv head) pairs need more partial records than the fixed
+    # array holds at head_dim 128 (6849 pairs on a 152-SM part); the call is
+    # refused on the host, before any launch
+    need = tq.tq_decode_attention_workspace_size(128, 64, 1 << 20, 128)
     assert need > SCRATCH_BYTES
-    q = torch.zeros((64, 64, 1, 128), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((128, 64, 1, 128), dtype=torch.bfloat16, device="cuda")
     one = torch.zeros(16, dtype=torch.uint8, device="cuda")
     p = one.data_ptr()
-    st = L.tq_decode_attention_noalloc(q.data_ptr(), 64, 64, 1, p, p, p, p, p, 64, 1 << 20, 128, 1 << 20, 8, 1, 3,
-                                       None, ctypes.c_float(0.1), p, 0, None)
+    st = L.tq_decode_attention_noalloc(q.data_ptr(), 128, 64, 1, p, p, p, p, p, 64, 1 << 20, 128, 1 << 20, 8, 1,
+                                       3, None, ctypes.c_float(0.1), p, 0, None)
     assert st == 1  # TQ_ERR_INVALID_ARG
+
+
+def test_noalloc_empty_batch_is_a_no_op(L):
+    """B == 0 returns TQ_OK like the workspace entry point, whatever the head_dim."""
+    for D in (64, 128, 256):
+        q = torch.zeros((1, 8, 1, D), dtype=torch.bfloat16, device="cuda")
+        one = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        p = one.data_ptr()
+        st = L.tq_decode_attention_noalloc(q.data_ptr(), 0, 8, 1, p, p, p, p, p, 8, 64, D, 64, 8, 1, 3, None,
+                                           ctypes.c_float(0.1), p, 0, None)
+        assert st == 0, tq.tq_status_string(st)

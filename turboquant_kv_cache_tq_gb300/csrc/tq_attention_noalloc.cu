@@ -68,6 +68,11 @@ extern "C" tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64
                                                  int k_bits, int k_signed, int v_bits,
                                                  const int32_t* left_pad, float scale, void* out,
                                                  tq_dtype out_dtype, void* stream) {
+  // An empty batch launches nothing and needs no scratch: the workspace call's
+  // own checks and result.
+  if (B == 0)
+    return tq_decode_attention(q, B, Hq, Nq, k_codes, k_scales, k_zeros, v_codes, v_scales, Hkv, T, D, t_cap,
+                               k_bits, k_signed, v_bits, left_pad, scale, out, out_dtype, nullptr, 0, stream);
   const int64_t need = tq_decode_attention_workspace_size(B, Hkv, T, D);
   if (need < 0) return static_cast<tq_status>(-need);
   if (need > tq::kNoAllocScratchBytes) return TQ_ERR_INVALID_ARG;  // beyond the fixed scratch
