@@ -714,7 +714,7 @@ def host_link_floor(dev, reps: int):
         print("host link, %s: %.2f ms per 32 layers, %.0f GB/s per direction" % (what, ms, total / ms / 1e6))
 
 
-def run_case(name: str, reps: int, v_bits=None):
+def run_case(name: str, reps: int, v_bits=None, batch=None):
     """A small fixed case for profiling one kernel with ncu: the codec on one
     workload (encode then decode, `reps` times), one fused decode-attention
     step over the long-context cache shape, or the plain-copy floor of the
@@ -753,9 +753,10 @@ def run_case(name: str, reps: int, v_bits=None):
         print("attention [32,8,8256,128] k8s v3: %.1f us" % _median_us(e))
         return
     w = WORKLOADS[name]
-    k, v = make_kv(w, device=dev)
+    B = w.B if batch is None else batch
+    k, v = make_kv(w, device=dev, B=B)
     vb = w.v_bits[0] if v_bits is None else v_bits
-    cache = tq.alloc_cache(w.B, w.H, w.t_cap or w.T, w.D, w.k_bits, vb, device=dev)
+    cache = tq.alloc_cache(B, w.H, w.t_cap or w.T, w.D, w.k_bits, vb, device=dev)
     ko, vo = torch.empty_like(k), torch.empty_like(v)
     torch.cuda.synchronize()
     for r in range(reps):
@@ -764,7 +765,7 @@ def run_case(name: str, reps: int, v_bits=None):
         tq.tq_decode_kv(cache, w.T, w.k_bits, w.k_signed, vb, k_out=ko, v_out=vo)
         e[r][1].record()
     torch.cuda.synchronize()
-    print("%s v%d encode+decode: %.1f us" % (name, vb, _median_us(e)))
+    print("%s B=%d v%d encode+decode: %.1f us" % (name, B, vb, _median_us(e)))
 
 
 def _median_us(events) -> float:
@@ -787,9 +788,10 @@ def main(argv=None):
                     help="profiling aid: run one small case (a workload name, 'attention', 'copy_floor' or 'host_link') --reps times")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--v-bits", type=int, default=None, help="value bits of a --case workload")
+    ap.add_argument("--batch", type=int, default=None, help="batch size of a --case workload (a smaller capture)")
     args = ap.parse_args(argv)
     if args.case:
-        run_case(args.case, args.reps, args.v_bits)
+        run_case(args.case, args.reps, args.v_bits, args.batch)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

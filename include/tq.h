@@ -287,6 +287,16 @@ tq_status tq_lloyd_max_fit_status(const void* workspace, void* stream);
  * [2, 256]. */
 int64_t tq_lloyd_max_fit_workspace_size(int levels);
 
+/* Device-side failures of the library's kernels on the current device (no
+ * counterpart on the pages: failure detection of this library). Kernels that
+ * wait on an asynchronous copy (the decode's bulk-copy path) bound the wait;
+ * one that gives up sets the device error word, stops early and leaves its
+ * outputs incomplete. This call waits for `stream`, then returns TQ_OK, or
+ * TQ_ERR_TIMEOUT once for each time the word was found set (it is cleared),
+ * or TQ_ERR_CUDA if the wait or the copies failed. The first decode on a
+ * device looks up the word's address (make it before any stream capture). */
+tq_status tq_device_status(void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* tq_status_string(int status);
 

@@ -44,6 +44,32 @@ def test_all_combinations(D, v_bits, dtype):
         check_roundtrip(k, v, kb, ks, v_bits)
 
 
+# ---- the bulk-copy decode (whole, 16-byte aligned tiles; bf16 outputs) ------------
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+@pytest.mark.parametrize("v_bits", [2, 3, 4, 5, 8])
+def test_bulk_decode_all_combinations(D, v_bits):
+    """Token counts that are whole tiles (multiples of 32 / (D / 32) rows) and
+    caches whose rows keep every tile 16-byte aligned take the decode with
+    bulk asynchronous copies: every key mode, full and spare capacity, eager
+    and rotated values, against the oracle; the device error word stays
+    clear."""
+    rpw = 32 // (D // 32)
+    T = rpw * {64: 7, 128: 9, 256: 5, 512: 6}[D]
+    for i, (kb, ks) in enumerate(KEY_MODES):
+        k = _rand((2, 3, T, D), torch.bfloat16, 500 + i + D + v_bits)
+        v = _rand((2, 3, T, D), torch.bfloat16, 600 + i + D + v_bits, scale=2.0)
+        check_roundtrip(k, v, kb, ks, v_bits)
+        check_roundtrip(k, v, kb, ks, v_bits, t_cap=T + 2 * rpw)
+        ref = oracle_encode(k, v, kb, ks, v_bits, t_cap=T + 2 * rpw)
+        dev = cache_from_numpy(ref)
+        kg, vg = tq.tq_decode_kv_rotated(dev, T, kb, ks, v_bits, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        kr, vr = oracle.decode_kv(ref, T, kb, ks, v_bits, out_dtype=oracle.BF16, rotated_v=True)
+        assert np.array_equal(vg.cpu().view(torch.int16).numpy().view(np.uint16), vr)
+        assert np.array_equal(kg.cpu().view(torch.int16).numpy().view(np.uint16), kr)
+    assert tq.lib().tq_device_status(None) == 0
+
+
 # ---- workloads at reduced size, element by element --------------------------------
 def test_tiny_workload_constant_group():
     w = WORKLOADS["tiny"]

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.tq_lloyd_max_fit_status.argtypes = [P, P]
             L.tq_lloyd_max_fit_workspace_size.restype = I64
             L.tq_lloyd_max_fit_workspace_size.argtypes = [I]
+            L.tq_device_status.restype = I
+            L.tq_device_status.argtypes = [P]
             L.tq_status_string.restype = ctypes.c_char_p
             L.tq_status_string.argtypes = [I]
             _lib = L

@@ -7,6 +7,7 @@
 // status code returned before any launch.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/tq.h"
 #include "tq_device.cuh"
@@ -24,6 +25,32 @@ int sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+namespace {
+
+// The library's device error word: kernels whose bounded waits give up set a
+// bit here (bit 0: a decode stage never arrived); read and cleared by
+// tq_device_status. Its device address is looked up once per device.
+__device__ unsigned g_device_error;
+std::mutex g_err_mutex;
+unsigned* g_err_ptr[128] = {nullptr};
+
+}  // namespace
+
+unsigned* device_error_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
 }
 
 namespace {
@@ -183,6 +210,7 @@ tq_status decode_impl(const void* k_codes, const void* k_scales, const void* k_z
   p.rot_scale = rotation_scale(D);
   p.tdiv = make_fast_div(static_cast<int>(T));
   p.neg_zero = -0.0f;
+  p.err = device_error_word();
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -335,6 +363,21 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
     default: e = launch_attention<256>(p, v_bits, kmode, bf16, s); break;
   }
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_device_status(void* stream) {
+  unsigned* err = device_error_word();
+  if (err == nullptr) return TQ_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ERR_CUDA;
+    return TQ_ERR_TIMEOUT;
+  }
+  return TQ_OK;
 }
 
 extern "C" const char* tq_status_string(int status) {

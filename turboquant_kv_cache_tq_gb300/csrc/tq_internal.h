@@ -51,6 +51,7 @@ struct DecodeParams {
   float neg_zero;       // -0.0f
   int pdk, pdv;         // bytes of a packed K / V row
   int ng;               // groups per row (D / 32)
+  unsigned* err;        // the library's device error word (bit 0: a bounded wait gave up), or null
 };
 
 struct UnrotateParams {
@@ -116,5 +117,9 @@ cudaError_t launch_lloyd_max_index(const float* u, long long n, int v_bits, uint
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+
+// Device address of the library's device error word on the current device
+// (looked up on first use per device), or null if the lookup failed.
+unsigned* device_error_word();
 
 }  // namespace tq

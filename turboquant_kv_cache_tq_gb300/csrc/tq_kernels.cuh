@@ -137,18 +137,32 @@ struct EncodeShape {
 };
 
 // Lloyd-Max index of the pair y * inv from the lane's replica of the compact
-// cell table (rep_lane = table + 8 (lane % 16) bytes): the same cell and
-// comparison as lm_index2_scaled, with the cell clamped into the range.
+// cell table: the same cell and comparison as lm_index2_scaled. No clamp is
+// needed: for a finite RMS every element of the group has |y| <= sqrt(32) rms
+// exactly, and the fp32 sum of squares, square root, eps and reciprocal move
+// that bound by at most a dozen unit roundoffs (less still when eps
+// dominates), so |y * inv| < sqrt(32) (1 + 2^-20) < 5.6569 and the cell
+// rint(v S) lies within +-R of OFF (R = floor(5.6569 S) + 1). `rep_bias` is
+// the shared-memory address of the lane's entry of the range's first cell
+// minus (kMagicBits + kLo) * 128 (mod 2^32): the entry of a cell is then one
+// multiply-add of the rounded value's bits away.
+__device__ __forceinline__ CellEntry ld_cell_shared(uint32_t addr) {
+  CellEntry e;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(e.b), "=r"(e.base) : "r"(addr));
+  return e;
+}
+
 template <int VB>
-__device__ __forceinline__ void lm_index2_rep(float2 y, float inv, const uint8_t* rep_lane, uint32_t& i0,
-                                              uint32_t& i1) {
+__device__ __forceinline__ uint32_t rep_bias_for(uint32_t rep_lane_sh) {
+  return rep_lane_sh - (kMagicBits + static_cast<uint32_t>(RepCells<VB>::kLo)) * 128u;
+}
+
+template <int VB>
+__device__ __forceinline__ void lm_index2_rep(float2 y, float inv, uint32_t rep_bias, uint32_t& i0, uint32_t& i1) {
   using G = CellGrid<VB>;
-  using RC = RepCells<VB>;
   const float2 s = fma2(y, f2(__fmul_rn(inv, G::S)), f2(grid_magic<VB>()));
-  const uint32_t r0 = min(__float_as_uint(s.x) - (kMagicBits + RC::kLo), static_cast<uint32_t>(RC::kCount - 1));
-  const uint32_t r1 = min(__float_as_uint(s.y) - (kMagicBits + RC::kLo), static_cast<uint32_t>(RC::kCount - 1));
-  const CellEntry e0 = *reinterpret_cast<const CellEntry*>(rep_lane + 128u * r0);
-  const CellEntry e1 = *reinterpret_cast<const CellEntry*>(rep_lane + 128u * r1);
+  const CellEntry e0 = ld_cell_shared(__float_as_uint(s.x) * 128u + rep_bias);
+  const CellEntry e1 = ld_cell_shared(__float_as_uint(s.y) * 128u + rep_bias);
   const float2 d = fma2(y, f2(-inv), make_float2(e0.b, e1.b));
   i0 = static_cast<uint32_t>(e0.base) + (__float_as_uint(d.x) >> 31);
   i1 = static_cast<uint32_t>(e1.base) + (__float_as_uint(d.y) >> 31);
@@ -372,8 +386,8 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
 // the caller) instead of the block's shared table.
 template <int LPR, int VB, bool F32, bool REP, bool SIGNS_IN_REGS, typename Prefetch>
 __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const uint32_t* s_sign,
-                                                  const void* s_cells, float rot_scale, float neg_zero,
-                                                  bool store, uint8_t* codes, uint16_t* scale_out,
+                                                  const void* s_cells, uint32_t rep_bias, float rot_scale,
+                                                  float neg_zero, bool store, uint8_t* codes, uint16_t* scale_out,
                                                   Prefetch&& prefetch) {
   uint32_t S[16];
   if constexpr (SIGNS_IN_REGS) {
@@ -403,7 +417,7 @@ __device__ __forceinline__ void encode_value_item(ItemIn<F32>& in, int l, const 
     // every group of the warp has a finite RMS: cells are in range unmasked
     pack_pairs<VB, false>(w, [&](int q, uint32_t& lo, uint32_t& hi) {
       if constexpr (REP) {
-        lm_index2_rep<VB>(Y[q], inv, static_cast<const uint8_t*>(s_cells), lo, hi);
+        lm_index2_rep<VB>(Y[q], inv, rep_bias, lo, hi);
       } else {
         lm_index2_scaled<VB, false>(Y[q], inv, static_cast<const CellEntry*>(s_cells), lo, hi);
       }
@@ -458,8 +472,10 @@ __global__ void __launch_bounds__(EncodeShape<D, VB, F32, ALLOW_REP>::kBlockThre
 
   const ItemOrder<SNAKE> ord{n_warps, gw, tiles};
   using R = typename SH::Ring;
-  const void* cells = SH::REP ? static_cast<const void*>(s_ring + R::kBlockBytes + 8 * (lane & 15))
-                              : static_cast<const void*>(s_cells);
+  const void* cells = static_cast<const void*>(s_cells);
+  const uint32_t rep_bias =
+      SH::REP ? rep_bias_for<VB>(static_cast<uint32_t>(__cvta_generic_to_shared(s_ring + R::kBlockBytes + 8 * (lane & 15))))
+              : 0u;
   uint8_t* lane_ring = s_ring + (threadIdx.x >> 5) * (R::kStages * R::kStageBytes) + lane * R::kLaneBytes;
   const uint32_t lane_ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(lane_ring));
   const int swz = R::swz(lane);
@@ -518,7 +534,7 @@ __global__ void __launch_bounds__(EncodeShape<D, VB, F32, ALLOW_REP>::kBlockThre
       encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l,
                                   p.k_scales + orow * NG + l, p.k_zeros + orow * NG + l, no_prefetch);
     } else {
-      encode_value_item<G::LPR, VB, F32, SH::REP, kRegSigns>(in, l, signs, cells, p.rot_scale, p.neg_zero, valid,
+      encode_value_item<G::LPR, VB, F32, SH::REP, kRegSigns>(in, l, signs, cells, rep_bias, p.rot_scale, p.neg_zero, valid,
                                          p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l,
                                          no_prefetch);
     }
@@ -652,14 +668,15 @@ __device__ __forceinline__ float centroid_at(const float* cent, const uint32_t (
   return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(cent) + byte_off);
 }
 
-// V decode of one group. ROT: leave the values in the rotated domain
-// (dequantScaled / decodeValuesRotated: centroid * scale only). SIGNS_IN_REGS:
-// s_sign is the lane's own 16 sign words (held in registers by the caller)
-// instead of the block's shared table.
+// V decode of one group into its output words: 16 words of bf16 pairs or 32
+// fp32 values, in element order. ROT: leave the values in the rotated domain
+// (dequantScaled / decodeValuesRotated: centroid * scale only).
+// SIGNS_IN_REGS: s_sign is the lane's own 16 sign words (held in registers by
+// the caller) instead of the block's shared table.
 template <int LPR, int VB, bool F32, bool ROT, bool SIGNS_IN_REGS, int W, typename Prefetch>
-__device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, const uint32_t* s_sign,
-                                                  const float* s_cent, float rot_scale, float neg_zero,
-                                                  bool store, void* out, size_t out_off, Prefetch&& prefetch) {
+__device__ __forceinline__ void decode_value_words(const PackedIn<W>& in, int l, const uint32_t* s_sign,
+                                                   const float* s_cent, float rot_scale, float neg_zero,
+                                                   uint32_t (&o)[F32 ? 32 : 16], Prefetch&& prefetch) {
   const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz & 0xffffu)));
   const float2 nz = f2(neg_zero);
   float2 Y[16];
@@ -689,10 +706,8 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
       load_sign_words(s_sign, l, S);
     }
   }
-  if (!store) return;
   if constexpr (!F32) {
     // round to bf16, then apply the signs on the packed words (exact)
-    uint32_t o[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const __nv_bfloat162 a = __floats2bfloat162_rn(Y[2 * j].x, Y[2 * j + 1].x);
@@ -700,15 +715,24 @@ __device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, 
       o[j] = *reinterpret_cast<const uint32_t*>(&a) ^ S[j];
       o[j + 8] = *reinterpret_cast<const uint32_t*>(&b) ^ S[j + 8];
     }
-    uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + out_off);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
   } else {
-    float x[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(S, i));
-    store_group<true>(out, out_off, x);
+    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(pair_elem(Y, i)) ^ elem_sign(S, i);
   }
+}
+
+// The same, stored to out + out_off (elements) when `store`.
+template <int LPR, int VB, bool F32, bool ROT, bool SIGNS_IN_REGS, int W, typename Prefetch>
+__device__ __forceinline__ void decode_value_item(const PackedIn<W>& in, int l, const uint32_t* s_sign,
+                                                  const float* s_cent, float rot_scale, float neg_zero,
+                                                  bool store, void* out, size_t out_off, Prefetch&& prefetch) {
+  uint32_t o[F32 ? 32 : 16];
+  decode_value_words<LPR, VB, F32, ROT, SIGNS_IN_REGS>(in, l, s_sign, s_cent, rot_scale, neg_zero, o, prefetch);
+  if (!store) return;
+  constexpr int kElem = F32 ? 4 : 2;
+  uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(out) + out_off * kElem);
+#pragma unroll
+  for (int i = 0; i < (F32 ? 8 : 4); ++i) q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
 // Decode staging, a template argument chosen per launch like the encode's
@@ -872,8 +896,17 @@ cudaError_t launch_encode_t(const EncodeParams& p, cudaStream_t s) {
   return launch_encode_shape<D, VB, KMODE, F32, false, false>(p, s, grid);
 }
 
+}  // namespace tq
+
+#include "tq_decode_bulk.cuh"
+
+namespace tq {
+
 template <int D, int VB, int KMODE, bool F32, bool ROT>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
+  if constexpr (!F32) {
+    if (bulk_decode_ok<D>(p, true)) return launch_decode_bulk<D, VB, KMODE, ROT>(p, s);
+  }
   static const int resident = std::min(resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT, false>),
                                        resident_blocks(decode_kernel<D, VB, KMODE, F32, ROT, true>));
   const long long items = 2LL * ((p.rows + Geo<D>::RPW - 1) / Geo<D>::RPW);
