@@ -145,7 +145,8 @@ tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx
  *            aligned) for the partial results of the split pass (one record
  *            per split block and kv head it covers); it must not be in use by
  *            another call still running, and needs no initialisation.
- * Limits: D in {64, 128, 256} (else TQ_ERR_HEAD_DIM); Hq a multiple of Hkv
+ * Limits: D in {64, 128, 256, 512} (else TQ_ERR_HEAD_DIM; at 512 two warps
+ * share each token tile, one per half of head_dim); Hq a multiple of Hkv
  * and (Hq / Hkv) * Nq <= 16 (else TQ_ERR_INVALID_ARG); t_cap % 16 == 0
  * (else TQ_ERR_ALIGNMENT). B == 0 is a no-op. Two kernels are enqueued on
  * `stream`: the split pass, which cuts the (batch, kv head, 16-token tile)
@@ -182,8 +183,8 @@ int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, in
  *     16 * (D + 2) floats per split block and per (batch, kv head) pair, with
  *     at most 8 split blocks per SM, so the largest B * Hkv served is
  *     floor(TQ_ATTENTION_NOALLOC_SCRATCH_BYTES / (64 * (D + 2))) - 8 * SMs:
- *     on a 152-SM GB300 that is 14671, 6849 and 2848 pairs at head_dim 64,
- *     128 and 256, independent of the number of tokens.
+ *     on a 152-SM GB300 that is 14671, 6849, 2848 and 824 pairs at head_dim
+ *     64, 128, 256 and 512, independent of the number of tokens.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture. TQ_ERR_CUDA if the lookup fails.

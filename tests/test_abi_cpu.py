@@ -156,7 +156,7 @@ def _attn(L, D=128, B=2, Hq=8, Hkv=2, Nq=1, T=20, t_cap=32, kb=8, ks=1, vb=3, dt
 
 
 def test_attention_argument_checks(L):
-    assert _attn(L, D=512) == HEAD_DIM and _attn(L, D=96) == HEAD_DIM
+    assert _attn(L, D=1024) == HEAD_DIM and _attn(L, D=96) == HEAD_DIM
     assert _attn(L, vb=6) == BITS and _attn(L, kb=4, ks=1) == BITS
     assert _attn(L, dtype=5) == DTYPE
     assert _attn(L, Hq=6, Hkv=4) == INVALID            # Hq not a multiple of Hkv
@@ -177,7 +177,8 @@ def test_attention_argument_checks(L):
 
 
 def test_attention_workspace_size(L):
-    assert L.tq_decode_attention_workspace_size(2, 2, 100, 512) == -HEAD_DIM
+    assert L.tq_decode_attention_workspace_size(2, 2, 100, 1024) == -HEAD_DIM
+    assert L.tq_decode_attention_workspace_size(2, 2, 100, 512) % (16 * (512 + 2) * 4) == 0
     assert L.tq_decode_attention_workspace_size(-1, 2, 100, 128) == -INVALID
     assert L.tq_decode_attention_workspace_size(2, 0, 100, 128) == -INVALID
     rec = 16 * (128 + 2) * 4

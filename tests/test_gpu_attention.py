@@ -90,12 +90,13 @@ def run_case(B, Hkv, G, Nq, T, D, kb, ks, vb, t_cap=None, left_pad=None, seed=0,
     return got, want, vmax, rc, q
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
 @pytest.mark.parametrize("vb", [2, 3, 4, 5, 8])
 def test_matches_oracle_all_widths(D, vb):
     """Every key mode and value width; ragged token counts spanning several
-    16-token tiles and several split blocks."""
-    T = {64: 203, 128: 141, 256: 77}[D]
+    16-token tiles and several split blocks. At head_dim 512 two warps share
+    each tile, one per half of head_dim."""
+    T = {64: 203, 128: 141, 256: 77, 512: 53}[D]
     for i, (kb, ks) in enumerate(KEY_MODES):
         got, want, vmax, _, _ = run_case(2, 2, 4, 1, T, D, kb, ks, vb, seed=10 * i + D + vb)
         compare_attention(got.cpu().numpy(), want, vmax, 4, "D%d k%d%s v%d" % (D, kb, "s" if ks else "", vb))
@@ -107,6 +108,19 @@ def test_query_rows_and_causal_tail(G, Nq):
     (query n sees keys <= T - Nq + n), one and two query-row tiles."""
     got, want, vmax, _, _ = run_case(2, 3, G, Nq, 90, 128, 8, True, 3, seed=G * 7 + Nq)
     compare_attention(got.cpu().numpy(), want, vmax, G, "G%d Nq%d" % (G, Nq))
+
+
+@pytest.mark.parametrize("G,Nq,pads", [(4, 1, None), (8, 2, [0, 33, 70]), (16, 1, [5, 0, 90]), (3, 5, None)])
+def test_head_dim_512_query_rows_and_pads(G, Nq, pads):
+    """head_dim 512 (a warp pair per tile, partial scores added through shared
+    memory) with one and two query-row tiles, causal tails and left pads."""
+    got, want, vmax, _, _ = run_case(3, 2, G, Nq, 90, 512, 8, True, 4, left_pad=pads, seed=G * 11 + Nq)
+    compare_attention(got.cpu().numpy(), want, vmax, G, "D512 G%d Nq%d pads %s" % (G, Nq, pads))
+    got, want, vmax, _, _ = run_case(3, 2, G, Nq, 90, 512, 4, False, 3, left_pad=pads, seed=G * 13 + Nq,
+                                     out_dtype=torch.bfloat16)
+    ref = oracle.f32_to_bf16_bits(want.astype(np.float32))
+    d = np.abs(oracle.bf16_bits_to_f32(_bits(got)).astype(np.float64) - oracle.bf16_bits_to_f32(ref))
+    assert np.all(d <= 2.0 ** -7 * np.abs(want) + ATTN_TOL * np.repeat(vmax, G, axis=1)[:, :, None, None])
 
 
 @pytest.mark.parametrize("pads", [[0, 5, 17, 63], [16, 1, 40, 0], [89, 0, 3, 90]])
@@ -227,9 +241,9 @@ def test_host_checks_on_device_tensors():
     with pytest.raises(tq.TQError):  # 8 heads per kv head x 3 tokens > 16 rows
         tq.tq_decode_attention(torch.zeros((1, 16, 3, 128), dtype=torch.bfloat16, device="cuda"), cache, 20,
                                8, True, 3)
-    cache512 = tq.alloc_cache(1, 2, 32, 512, 8, 3)
-    with pytest.raises(tq.TQError) as e:
-        tq.tq_decode_attention(torch.zeros((1, 2, 1, 512), dtype=torch.bfloat16, device="cuda"), cache512, 20,
+    cache1k = tq.alloc_cache(1, 2, 32, 1024, 8, 3)
+    with pytest.raises(tq.TQError) as e:  # head_dim 1024 is not a TurboQuant head dim
+        tq.tq_decode_attention(torch.zeros((1, 2, 1, 1024), dtype=torch.bfloat16, device="cuda"), cache1k, 20,
                                8, True, 3)
     assert e.value.status == 2
 

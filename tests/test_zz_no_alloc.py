@@ -67,7 +67,7 @@ def _vrot_max(cache, T, kb, ks, vb):
 
 def test_noalloc_matches_workspace_entry_point_twice(L):
     cases = [(4, 8, 4, 1000, 128, 8, True, 3, 1), (2, 4, 2, 333, 64, 4, False, 5, 2),
-             (3, 8, 2, 517, 256, 8, True, 4, 3)]
+             (3, 8, 2, 517, 256, 8, True, 4, 3), (2, 4, 4, 211, 512, 8, True, 5, 4)]
     for (B, Hkv, G, T, D, kb, ks, vb, seed) in cases:
         q, cache, lp, t_cap = _case(B, Hkv, G, T, D, kb, ks, vb, seed)
         assert tq.tq_decode_attention_workspace_size(B, Hkv, T, D) <= SCRATCH_BYTES
@@ -98,7 +98,7 @@ def test_noalloc_refuses_sizes_beyond_the_scratch(L):
 
 def test_noalloc_empty_batch_is_a_no_op(L):
     """B == 0 returns TQ_OK like the workspace entry point, whatever the head_dim."""
-    for D in (64, 128, 256):
+    for D in (64, 128, 256, 512):
         q = torch.zeros((1, 8, 1, D), dtype=torch.bfloat16, device="cuda")
         one = torch.zeros(16, dtype=torch.uint8, device="cuda")
         p = one.data_ptr()

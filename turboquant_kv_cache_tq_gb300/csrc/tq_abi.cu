@@ -289,7 +289,7 @@ namespace {
 // touches, at most kAttnGridPerSm blocks per SM plus one per (batch, kv head).
 long long attn_records(long long bhkv) { return static_cast<long long>(kAttnGridPerSm) * sm_count() + bhkv; }
 
-bool attn_head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256; }
+bool attn_head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
 }  // namespace
 }  // namespace tq
@@ -360,7 +360,8 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   switch (D) {
     case 64: e = launch_attention<64>(p, v_bits, kmode, bf16, s); break;
     case 128: e = launch_attention<128>(p, v_bits, kmode, bf16, s); break;
-    default: e = launch_attention<256>(p, v_bits, kmode, bf16, s); break;
+    case 256: e = launch_attention<256>(p, v_bits, kmode, bf16, s); break;
+    default: e = launch_attention<512>(p, v_bits, kmode, bf16, s); break;
   }
   return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

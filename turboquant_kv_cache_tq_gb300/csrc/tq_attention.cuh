@@ -71,10 +71,6 @@ struct AttnLayout {
   // 4 bits, once per half-warp lane; single centroids once per lane above
   static constexpr int CENT = VB <= 4 ? (16 * 8) << (2 * VB) : (32 * 4) << VB;
   static constexpr int RING = kAttnWarps * STAGES * STAGE;
-  static constexpr int REC = kAttnRows * (D + 2);  // floats of a partial record: m[16], l[16], O[16][D]
-  static_assert(REC == kAttnRecordFloats(D), "record layout shared with the host");
-  static constexpr int MERGE = kAttnWarps * REC * 4;
-  static constexpr int SMEM = CENT + (RING > MERGE ? RING : MERGE);
   // per-lane element ranges
   static constexpr int EK = D / 4;  // keys: token g, elements [c EK, (c+1) EK)
   static constexpr int EV = D / 8;  // values: elements [g EV, (g+1) EV) of four tokens
@@ -84,6 +80,51 @@ struct AttnLayout {
   static constexpr bool VALIGN = (EV * VB / 8) % 4 == 0;
   static constexpr int KGROUPS = EK > kGroup ? EK / kGroup : 1;  // groups a lane's key range spans
 };
+
+// Head_dim split: at D = 512 a warp's registers cannot hold a whole row's
+// query operands and output accumulators, so two warps share each token tile,
+// one per half of head_dim: each decodes its half of the keys and values,
+// their partial scores are added through shared memory (both add the same two
+// terms, so both get the same scores and the same softmax), and each keeps
+// the output accumulators of its half. SPL warps per tile, DH elements each.
+template <int D>
+struct AttnSplit {
+  static constexpr int SPL = D == 512 ? 2 : 1;
+  static constexpr int DH = D / SPL;
+};
+
+// Block-level shared memory of the split kernel over the per-warp layout L:
+// value table | score exchange (SPL = 2) | ring of stages, later the merge
+// area of one record per warp group.
+template <int D, int KB, int VB, int NT>
+struct AttnSmem {
+  using L = AttnLayout<AttnSplit<D>::DH, KB, VB>;
+  static constexpr int SPL = AttnSplit<D>::SPL;
+  static constexpr int REC = kAttnRows * (D + 2);  // floats of a partial record: m[16], l[16], O[16][D]
+  static_assert(REC == kAttnRecordFloats(D), "record layout shared with the host");
+  static constexpr int MERGE = (kAttnWarps / SPL) * REC * 4;
+  // two slots (tile parity) x warps x 32 lanes x NT x 4 partial scores
+  static constexpr int XCHG = SPL > 1 ? 2 * kAttnWarps * 32 * NT * 4 * 4 : 0;
+  static constexpr int XOFF = L::CENT;
+  static constexpr int WORK = XOFF + XCHG;
+  static constexpr int SMEM = WORK + (L::RING > MERGE ? L::RING : MERGE);
+};
+
+// Copy ROWS rows of HB bytes (a multiple of 16) taken at a stride of FB bytes
+// from global memory into ROWS x HB contiguous bytes of shared memory, with the
+// warp's 16-byte asynchronous copies.
+template <int ROWS, int HB, int FB>
+__device__ __forceinline__ void copy_rows(uint32_t dst, const void* src, int lane) {
+  static_assert(HB % 16 == 0 && FB % 16 == 0, "16-byte pieces");
+  constexpr int PR = HB / 16;
+  const char* s = static_cast<const char*>(src);
+#pragma unroll
+  for (int i = lane; i < ROWS * PR; i += 32) cp_async16(dst + 16 * i, s + (i / PR) * FB + 16 * (i % PR));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // NW little-endian words from byte `off` of shared memory (any byte offset
 // when !ALIGNED; reads up to 4 bytes past the last word).
@@ -198,17 +239,25 @@ template <int D, int VB, int KMODE, int NT>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) {
   using M = KeySpec<KMODE>;
   constexpr int KB = M::B;
-  using L = AttnLayout<D, KB, VB>;
+  using SM = AttnSmem<D, KB, VB, NT>;
+  using L = typename SM::L;  // the per-warp layout over DH head_dim elements
+  constexpr int SPL = SM::SPL;
+  constexpr int DH = AttnSplit<D>::DH;
+  constexpr int PDK_FULL = D * KB / 8, PDV_FULL = D * VB / 8, NG_FULL = D / kGroup;
   using VT = ValueTable<VB>;
   constexpr int S = L::STAGES;
   const float kNegInf = -__int_as_float(0x7f800000);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_vtab = smem;
-  uint8_t* s_work = smem + L::CENT;
+  float* s_xchg = reinterpret_cast<float*>(smem + SM::XOFF);
+  uint8_t* s_work = smem + SM::WORK;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int Rq = p.G * p.Nq;
+  const int team = warp / SPL;           // warps sharing a tile
+  const int half = warp % SPL;           // the head_dim slice of this warp
+  constexpr int kTeams = kAttnWarps / SPL;
 
   fill_value_table<VB>(s_vtab);
   pdl_launch_dependents();
@@ -234,14 +283,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     // head_dim elements c D/4 + 4 j .. + 3 for k-step j (the contraction's
     // permuted order: MMA k index kk of k-step j is element
     // (kk % 8 / 2) D/4 + 4 j + 2 (kk / 8) + kk % 2). Padding rows are zero.
-    uint32_t qf[D / 16][NT][2];
+    uint32_t qf[DH / 16][NT][2];
     {
-      const uint16_t* qsrc = p.q + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * p.G) * p.Nq * D;
+      const uint16_t* qsrc = p.q + (static_cast<long long>(b) * p.Hq + static_cast<long long>(h) * p.G) * p.Nq * D +
+                             half * DH;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const int row = 8 * n + g;
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
+        for (int j = 0; j < DH / 16; ++j) {
           uint2 u = make_uint2(0u, 0u);
           if (row < Rq) u = *reinterpret_cast<const uint2*>(qsrc + row * D + c * L::EK + 4 * j);
           qf[j][n][0] = u.x;
@@ -268,25 +318,34 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     uint8_t* ring = s_work + warp * S * L::STAGE;
     const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     const long long tok0 = static_cast<long long>(bh) * p.t_cap + t_beg;
-    const int my_tiles = n_tiles > warp ? (n_tiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
-    // Step k of this warp handles tile warp + 4 k in stage k mod S; every step
-    // commits one copy group (empty past the end).
+    const int my_tiles = n_tiles > team ? (n_tiles - team + kTeams - 1) / kTeams : 0;
+    // Step k of this warp handles tile team + kTeams k in stage k mod S (its
+    // half of each row when SPL = 2); every step commits one copy group
+    // (empty past the end).
     auto issue = [&](int k) {
       if (k < my_tiles) {
-        const long long t = tok0 + static_cast<long long>(warp + k * kAttnWarps) * kAttnTile;
+        const long long t = tok0 + static_cast<long long>(team + k * kTeams) * kAttnTile;
         const uint32_t dst = ring_sh + (k % S) * L::STAGE;
-        copy_region<kAttnTile * L::PDK>(dst + L::KC, p.k_codes + t * L::PDK, lane);
-        copy_region<kAttnTile * L::NG * 2>(dst + L::KS, p.k_scales + t * L::NG, lane);
-        copy_region<kAttnTile * L::NG * 2>(dst + L::KZ, p.k_zeros + t * L::NG, lane);
-        copy_region<kAttnTile * L::PDV>(dst + L::VC, p.v_codes + t * L::PDV, lane);
-        copy_region<kAttnTile * L::NG * 2>(dst + L::VS, p.v_scales + t * L::NG, lane);
+        if constexpr (SPL == 1) {
+          copy_region<kAttnTile * L::PDK>(dst + L::KC, p.k_codes + t * L::PDK, lane);
+          copy_region<kAttnTile * L::NG * 2>(dst + L::KS, p.k_scales + t * L::NG, lane);
+          copy_region<kAttnTile * L::NG * 2>(dst + L::KZ, p.k_zeros + t * L::NG, lane);
+          copy_region<kAttnTile * L::PDV>(dst + L::VC, p.v_codes + t * L::PDV, lane);
+          copy_region<kAttnTile * L::NG * 2>(dst + L::VS, p.v_scales + t * L::NG, lane);
+        } else {
+          copy_rows<kAttnTile, L::PDK, PDK_FULL>(dst + L::KC, p.k_codes + t * PDK_FULL + half * L::PDK, lane);
+          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::KS, p.k_scales + t * NG_FULL + half * L::NG, lane);
+          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::KZ, p.k_zeros + t * NG_FULL + half * L::NG, lane);
+          copy_rows<kAttnTile, L::PDV, PDV_FULL>(dst + L::VC, p.v_codes + t * PDV_FULL + half * L::PDV, lane);
+          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::VS, p.v_scales + t * NG_FULL + half * L::NG, lane);
+        }
       }
       cp_async_commit();
     };
 
-    float acc[D / 16][NT][4];
+    float acc[DH / 16][NT][4];
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i)
+    for (int i = 0; i < DH / 16; ++i)
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -310,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
       cp_async_wait<S - 1>();
       __syncwarp();
       const uint8_t* st = ring + (k % S) * L::STAGE;
-      const int t0 = t_beg + (warp + k * kAttnWarps) * kAttnTile;
+      const int t0 = t_beg + (team + k * kTeams) * kAttnTile;
       // a tile inside [t_lo, T - Nq] needs no mask (warp-uniform)
       const bool full = t0 >= t_lo && t0 + kAttnTile - 1 <= t_full;
 
@@ -344,7 +403,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[n][ch][e] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
+      for (int j = 0; j < DH / 16; ++j) {
         const int lg = (4 * j) / kGroup;
         uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
 #pragma unroll
@@ -377,6 +436,31 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
       }
 
+      // ---- the team's partial scores added (SPL = 2): each warp publishes
+      // its half's sums in slot k mod 2, and adds the other half's to its own
+      // (the same two terms in both warps, so the same sums)
+      float sfull[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sfull[n][e] = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
+      if constexpr (SPL > 1) {
+        float* slot = s_xchg + (k & 1) * (kAttnWarps * 32 * NT * 4);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) slot[((warp * NT + n) * 4 + e) * 32 + lane] = sfull[n][e];
+        named_barrier(1 + team, 32 * SPL);
+        const int other = warp ^ 1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float o = slot[((other * NT + n) * 4 + e) * 32 + lane];
+            sfull[n][e] = half == 0 ? __fadd_rn(sfull[n][e], o) : __fadd_rn(o, sfull[n][e]);
+          }
+      }
+
       // ---- online softmax per query column 8 n + 2 c + x (tokens g, g + 8
       // in entries x and 2 + x); the column's values sit in the eight lanes
       // with the same c
@@ -387,7 +471,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         float xs[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float sv = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
+          const float sv = sfull[n][e];
           if (full) {
             xs[e] = __fmul_rn(sv, p.scale_log2);
           } else {
@@ -418,7 +502,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         for (int n = 0; n < NT; ++n) change = change || al[n][0] != 1.0f || al[n][1] != 1.0f;
         if (__any_sync(kFull, change)) {
 #pragma unroll
-          for (int i = 0; i < D / 16; ++i)
+          for (int i = 0; i < DH / 16; ++i)
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
               acc[i][n][0] = __fmul_rn(acc[i][n][0], al[n][0]);
@@ -460,7 +544,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         vs2[k4] = f2(sc);
       }
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
+      for (int i = 0; i < DH / 16; ++i) {
         // elements 2i, 2i + 1 of each token: RN(centroid * scale), to bf16
         float2 v[4];
 #pragma unroll
@@ -494,10 +578,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         l_run[n][x] = __fadd_rn(l_run[n][x], __shfl_xor_sync(kFull, l_run[n][x], 16));
       }
 
-    // ---- merge the four warps in shared memory, one record per block
+    // ---- merge the teams in shared memory, one record per block (the
+    // warps of a team share m and l and each holds its half of O)
     __syncthreads();  // every warp is done with its ring
-    float* mine = reinterpret_cast<float*>(s_work) + warp * L::REC;
-    if (g == 0) {
+    float* mine = reinterpret_cast<float*>(s_work) + team * SM::REC;
+    if (g == 0 && half == 0) {
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -507,9 +592,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
         }
     }
     {
-      float* O = mine + 32;
+      float* O = mine + 32 + half * DH;
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i)
+      for (int i = 0; i < DH / 16; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           const int q0 = 8 * n + 2 * c, d0 = g * L::EV + 2 * i;
@@ -521,29 +606,29 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     }
     __syncthreads();
     const float* all = reinterpret_cast<const float*>(s_work);
-    float* rec = p.ws + (static_cast<long long>(blockIdx.x) + bh) * L::REC;
+    float* rec = p.ws + (static_cast<long long>(blockIdx.x) + bh) * SM::REC;
     for (int i = threadIdx.x; i < Rq * D; i += blockDim.x) {
       const int r = i / D;
       float mx = kNegInf;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
+      for (int w = 0; w < kTeams; ++w) mx = fmaxf(mx, all[w * SM::REC + r]);
       float sum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float mw = all[w * L::REC + r];
-        if (mw != kNegInf) sum = __fadd_rn(sum, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 32 + i]));
+      for (int w = 0; w < kTeams; ++w) {
+        const float mw = all[w * SM::REC + r];
+        if (mw != kNegInf) sum = __fadd_rn(sum, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * SM::REC + 32 + i]));
       }
       rec[32 + i] = sum;
     }
     for (int r = threadIdx.x; r < Rq; r += blockDim.x) {
       float mx = kNegInf;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, all[w * L::REC + r]);
+      for (int w = 0; w < kTeams; ++w) mx = fmaxf(mx, all[w * SM::REC + r]);
       float l = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float mw = all[w * L::REC + r];
-        if (mw != kNegInf) l = __fadd_rn(l, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * L::REC + 16 + r]));
+      for (int w = 0; w < kTeams; ++w) {
+        const float mw = all[w * SM::REC + r];
+        if (mw != kNegInf) l = __fadd_rn(l, __fmul_rn(exp2f(__fsub_rn(mw, mx)), all[w * SM::REC + 16 + r]));
       }
       rec[r] = mx;
       rec[16 + r] = l;
@@ -553,83 +638,106 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
 
 // Merge of the chunk partials of one output row, normalisation, inverse
 // rotation (unrotateValues: fp32 Hadamard butterflies, * 1/sqrt(D), signs)
-// and the store, with the codec's lane layout: lane l of a row owns elements
-// [32 l, 32 l + 32).
+// and the store. A block takes one tile of output rows in the codec's lane
+// layout (lane l of a row owns elements [32 l, 32 l + 32)); its warps split
+// the row's chunk records between them (warp w merges records w, w + NW,
+// ...), since a head spread over many split blocks has many records: first
+// the largest running max over every record, then each warp's weighted sum,
+// then warp 0 adds the warps' sums in order and finishes the row.
+constexpr int kCombineWarps = 8;
+
 template <int D, bool F32>
-__global__ void __launch_bounds__(kThreads) attn_combine_kernel(AttnParams p) {
+__global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnParams p) {
   using G = Geo<D>;
   constexpr int REC = kAttnRows * (D + 2);
+  constexpr int NW = kCombineWarps;
   const float kNegInf = -__int_as_float(0x7f800000);
   __shared__ __align__(16) uint32_t s_sign[D / 2];
+  __shared__ float s_max[NW][32];
+  __shared__ float s_part[NW][32][33];  // per warp and lane: 32 weighted sums and the denominator
   fill_sign_words<D>(s_sign);
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / G::LPR;
   const int l = lane % G::LPR;
-  const int n_warps = gridDim.x * (blockDim.x >> 5);
   const int rows = p.B * p.Hq * p.Nq;
-  const int tiles = (rows + G::RPW - 1) / G::RPW;
+  const int row0 = blockIdx.x * G::RPW + sub;
+  const bool valid = row0 < rows;
+  const int row = valid ? row0 : rows - 1;
+  const int hq_n = p.Hq * p.Nq;
+  const int b = row / hq_n;
+  const int rem = row - b * hq_n;
+  const int hq = rem / p.Nq, n = rem - (rem / p.Nq) * p.Nq;
+  const int h = hq / p.G;
+  const int r = (hq - h * p.G) * p.Nq + n;
+  // the split blocks that covered this head's tiles wrote records at slots
+  // (block + bh); block of tile x = floor(((x + 1) grid - 1) / total)
+  const int bh = b * p.Hkv + h;
+  int c0 = 0, n_rec = 0;
+  if (p.tiles_per_bh > 0) {
+    const long long x0 = static_cast<long long>(bh) * p.tiles_per_bh, x1 = x0 + p.tiles_per_bh - 1;
+    c0 = static_cast<int>(((x0 + 1) * p.grid - 1) / p.total_tiles);
+    n_rec = static_cast<int>(((x1 + 1) * p.grid - 1) / p.total_tiles) - c0 + 1;
+  }
+  const float* recs = p.ws + (static_cast<long long>(c0) + bh) * REC;
+  float mx = kNegInf;
+  for (int s = warp; s < n_rec; s += NW) mx = fmaxf(mx, recs[s * REC + r]);
+  s_max[warp][lane] = mx;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) mx = fmaxf(mx, s_max[w][lane]);
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+  float den = 0.0f;
+  for (int s = warp; s < n_rec; s += NW) {
+    const float* rec = recs + s * REC;
+    const float ms = rec[r];
+    if (ms == kNegInf) continue;
+    const float f = exp2f(__fsub_rn(ms, mx));
+    den = __fadd_rn(den, __fmul_rn(f, rec[16 + r]));
+    const float4* o = reinterpret_cast<const float4*>(rec + 32 + r * D + kGroup * l);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 u = o[i];
+      x[4 * i] = __fadd_rn(x[4 * i], __fmul_rn(f, u.x));
+      x[4 * i + 1] = __fadd_rn(x[4 * i + 1], __fmul_rn(f, u.y));
+      x[4 * i + 2] = __fadd_rn(x[4 * i + 2], __fmul_rn(f, u.z));
+      x[4 * i + 3] = __fadd_rn(x[4 * i + 3], __fmul_rn(f, u.w));
+    }
+  }
+  if (warp != 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s_part[warp][lane][i] = x[i];
+    s_part[warp][lane][32] = den;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __fadd_rn(x[i], s_part[w][lane][i]);
+    den = __fadd_rn(den, s_part[w][lane][32]);
+  }
   uint32_t Sg[16];
   load_sign_words(s_sign, l, Sg);
-  for (int tile = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < tiles; tile += n_warps) {
-    const int row0 = tile * G::RPW + sub;
-    const bool valid = row0 < rows;
-    const int row = valid ? row0 : rows - 1;
-    const int hq_n = p.Hq * p.Nq;
-    const int b = row / hq_n;
-    const int rem = row - b * hq_n;
-    const int hq = rem / p.Nq, n = rem - (rem / p.Nq) * p.Nq;
-    const int h = hq / p.G;
-    const int r = (hq - h * p.G) * p.Nq + n;
-    // the split blocks that covered this head's tiles wrote records at
-    // slots (block + bh); block of tile x = floor(((x + 1) grid - 1) / total)
-    const int bh = b * p.Hkv + h;
-    int c0 = 0, n_rec = 0;
-    if (p.tiles_per_bh > 0) {
-      const long long x0 = static_cast<long long>(bh) * p.tiles_per_bh, x1 = x0 + p.tiles_per_bh - 1;
-      c0 = static_cast<int>(((x0 + 1) * p.grid - 1) / p.total_tiles);
-      n_rec = static_cast<int>(((x1 + 1) * p.grid - 1) / p.total_tiles) - c0 + 1;
-    }
-    const float* recs = p.ws + (static_cast<long long>(c0) + bh) * REC;
-    float mx = kNegInf;
-    for (int s = 0; s < n_rec; ++s) mx = fmaxf(mx, recs[s * REC + r]);
-    float x[32];
+  // a row with no valid key is zero
+  const bool empty = den == 0.0f;
+  float2 Y[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-    float den = 0.0f;
-    for (int s = 0; s < n_rec; ++s) {
-      const float* rec = recs + s * REC;
-      const float ms = rec[r];
-      if (ms == kNegInf) continue;
-      const float f = exp2f(__fsub_rn(ms, mx));
-      den = __fadd_rn(den, __fmul_rn(f, rec[16 + r]));
-      const float4* o = reinterpret_cast<const float4*>(rec + 32 + r * D + kGroup * l);
+  for (int q = 0; q < 16; ++q)
+    Y[q] = empty ? make_float2(0.0f, 0.0f) : make_float2(__fdiv_rn(x[q], den), __fdiv_rn(x[q + 16], den));
+  hadamard_row<G::LPR>(Y, l);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 u = o[i];
-        x[4 * i] = __fadd_rn(x[4 * i], __fmul_rn(f, u.x));
-        x[4 * i + 1] = __fadd_rn(x[4 * i + 1], __fmul_rn(f, u.y));
-        x[4 * i + 2] = __fadd_rn(x[4 * i + 2], __fmul_rn(f, u.z));
-        x[4 * i + 3] = __fadd_rn(x[4 * i + 3], __fmul_rn(f, u.w));
-      }
-    }
-    // a row with no valid key is zero
-    const bool empty = den == 0.0f;
-    float2 Y[16];
+  for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], f2(p.rot_scale));
+  if (!valid) return;
+  float y[32];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      Y[q] = empty ? make_float2(0.0f, 0.0f) : make_float2(__fdiv_rn(x[q], den), __fdiv_rn(x[q + 16], den));
-    hadamard_row<G::LPR>(Y, l);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], f2(p.rot_scale));
-    if (!valid) continue;
-    float y[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(Sg, i));
-    store_group<F32>(p.out, static_cast<size_t>(row) * D + kGroup * l, y);
-  }
+  for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(__float_as_uint(pair_elem(Y, i)) ^ elem_sign(Sg, i));
+  store_group<F32>(p.out, static_cast<size_t>(row) * D + kGroup * l, y);
 }
 
 // Launch with programmatic stream serialization and a given block size.
@@ -652,7 +760,7 @@ inline cudaError_t launch_pdl_block(void (*kernel)(Params), int grid, int block,
 // Sets p.grid to the split grid it launches.
 template <int D, int VB, int KMODE, int NT>
 cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
-  using L = AttnLayout<D, KeySpec<KMODE>::B, VB>;
+  using L = AttnSmem<D, KeySpec<KMODE>::B, VB, NT>;
   static const cudaError_t attr = cudaFuncSetAttribute(attn_split_kernel<D, VB, KMODE, NT>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (attr != cudaSuccess) return attr;
@@ -703,13 +811,11 @@ cudaError_t launch_attention(const AttnParams& params, int v_bits, int kmode, bo
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Nq;
-  const long long tiles = (rows + Geo<D>::RPW - 1) / Geo<D>::RPW;
+  const int tiles = static_cast<int>((rows + Geo<D>::RPW - 1) / Geo<D>::RPW);  // one block per row tile
   if (out_bf16) {
-    static const int resident = resident_blocks(attn_combine_kernel<D, false>);
-    e = launch_pdl(attn_combine_kernel<D, false>, grid_for(tiles, resident), p, s);
+    e = launch_pdl(attn_combine_kernel<D, false>, tiles, p, s, 0, 32 * kCombineWarps);
   } else {
-    static const int resident = resident_blocks(attn_combine_kernel<D, true>);
-    e = launch_pdl(attn_combine_kernel<D, true>, grid_for(tiles, resident), p, s);
+    e = launch_pdl(attn_combine_kernel<D, true>, tiles, p, s, 0, 32 * kCombineWarps);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
