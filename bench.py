@@ -290,7 +290,8 @@ def codec_roofline(workload: str, vb: int, rows: int, D: int, kb: int, enc_us: f
     launches, plus both launch times."""
     bpl = rows * bytes_per_row(D, kb, vb, 2)
     name = "%s_v%d" % (workload, vb)
-    kernel, us = ("encode_kernel", enc_us) if enc_us >= dec_us else ("decode_kernel", dec_us)
+    # the benchmark workloads' decodes (bf16 outputs, whole aligned tiles) take the bulk-copy kernel
+    kernel, us = ("encode_kernel", enc_us) if enc_us >= dec_us else ("decode_bulk_kernel", dec_us)
     r = roofline_obj(kernel, name, bpl, us, peak, peak_kind)
     r["encode_us"], r["decode_us"] = r4(enc_us), r4(dec_us)
     r["encode_frac"] = r4(bpl / (enc_us * 1e-6) / 1e9 / peak)
@@ -450,9 +451,10 @@ def run_secondary(args, tq, dev, stream, peak, peak_kind, rank):
                 ms = _time_launches(g.replay, stream, 20)
                 out["append_v%d" % vb] = {"us_per_step": r4(1e3 * ms / len(steps)), "rows_per_step": w.B * w.H,
                                           "steps_per_graph": len(steps)}
-                out["attention_v%d" % vb] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, peak_kind)
                 if vb == 3:
                     out["batched_merge_v3"] = time_merge(tq, w, cache, t_cap, dev, stream, peak)
+            out["attention_%s_v%d" % (name, vb)] = time_attention(tq, w, cache, t_cap, vb, dev, stream, peak,
+                                                                  peak_kind)
             del cache
         del k, v, ko, vo
         torch.cuda.empty_cache()
@@ -520,9 +522,10 @@ def time_layers(tq, dev, stream, peak, peak_kind, rank):
 
 
 def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, peak_kind, G=4):
-    """One decode step of fused attention over the whole packed cache (all
-    t_cap tokens valid): Llama-3-8B's 4 query heads per kv head, one query
-    token per sequence. Algorithmic bytes: the packed cache, read once."""
+    """One decode step of fused attention over the whole packed cache of a
+    workload (all t_cap tokens valid): 4 query heads per kv head (as in
+    Llama-3-8B), one query token per sequence. Algorithmic bytes: the packed
+    cache, read once."""
     g = torch.Generator(device=dev).manual_seed(6)
     q = torch.randn((w.B, w.H * G, 1, w.D), generator=g, device=dev).to(torch.bfloat16)
     out = torch.empty_like(q)
@@ -532,7 +535,7 @@ def time_attention(tq, w, cache, t_cap, vb, dev, stream, peak, peak_kind, G=4):
                                                        workspace=work, stream=stream), stream, 10)
     rows = w.B * w.H * t_cap
     per_row = w.D * w.k_bits // 8 + w.D * vb // 8 + 3 * (w.D // 32) * 2
-    r = roofline_obj("attn_split_kernel", "long_context_attention_v%d" % vb, rows * per_row, 1e3 * ms, peak,
+    r = roofline_obj("attn_split_kernel", "%s_attention_v%d" % (w.name, vb), rows * per_row, 1e3 * ms, peak,
                      peak_kind)
     r["kv_tokens_per_s"] = r4(w.B * t_cap / (ms * 1e-3))
     r["query_heads"], r["kv_tokens"], r["launches"] = w.H * G, t_cap, 2
@@ -561,16 +564,32 @@ def time_lloyd(tq, dev, stream, n=1 << 20, iters=500):
     unit-normal sample) of 2^20 samples at 4 and 8 bits, in microseconds per
     iteration: the 4 MB sample stays in L2 and every iteration is a chain of
     dependent steps ending in a grid barrier, so HBM bandwidth is not its
-    bound."""
+    bound. Its floor, measured here too: the same fit on an empty sample (an
+    iteration is then its grid barrier, the cell-sum clearing and the means:
+    barrier_floor_us) plus one pass over the sample at the L2's streaming
+    rate (a 32 MB copy between buffers that stay in L2: l2_pass_us)."""
     g = torch.Generator(device=dev).manual_seed(7)
     x = torch.randn(n, generator=g, device=dev)
     out = {"samples": n, "iterations": iters}
+    empty = torch.empty(0, device=dev)
+    # the L2's streaming rate: a 32 MB copy between two buffers that stay in L2
+    a = torch.empty(8 << 20, device=dev)
+    b = torch.empty_like(a)
+    l2_ms = _time_launches(lambda: b.copy_(a), stream, 50)
+    l2_gbs = 2 * a.numel() * 4 / (l2_ms * 1e-3) / 1e9
+    l2_pass = 4 * n / (l2_gbs * 1e9) * 1e3  # ms to read the sample once at that rate
+    out["l2_GBps"] = r4(l2_gbs)
+    out["l2_pass_us"] = r4(1e3 * l2_pass)
     for bits in (4, 8):
         K = 1 << bits
         init = torch.linspace(-3.0, 3.0, K, device=dev)
         work = torch.empty(tq.lib().tq_lloyd_max_fit_workspace_size(K), dtype=torch.uint8, device=dev)
         ms = _time_launches(lambda: tq.tq_lloyd_max_fit(x, init, iters, workspace=work, stream=stream), stream, 3)
-        out["bits%d_us_per_iteration" % bits] = r4(1e3 * ms / iters)
+        ms0 = _time_launches(lambda: tq.tq_lloyd_max_fit(empty, init, iters, workspace=work, stream=stream),
+                             stream, 3)
+        us, floor = 1e3 * ms / iters, 1e3 * ms0 / iters + 1e3 * l2_pass
+        out["bits%d" % bits] = {"us_per_iteration": r4(us), "barrier_floor_us": r4(1e3 * ms0 / iters),
+                                "floor_us": r4(floor), "frac_of_floor": r4(floor / us)}
     return out
 
 

@@ -35,6 +35,14 @@
 
 #include <stdint.h>
 
+/* The entry points are the library's only exported symbols (it is built
+ * with hidden visibility for everything else). */
+#if defined(__GNUC__)
+#define TQ_API __attribute__((visibility("default")))
+#else
+#define TQ_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -48,7 +56,8 @@ typedef enum {
     TQ_ERR_ALIGNMENT = 4,   /* dim*bits not a multiple of 8; a buffer not 16-byte aligned */
     TQ_ERR_DTYPE = 5,       /* unknown tq_dtype */
     TQ_ERR_CUDA = 6,        /* the CUDA runtime reported an error */
-    TQ_ERR_TIMEOUT = 7      /* a bounded device-side wait gave up (tq_lloyd_max_fit_status) */
+    TQ_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (tq_lloyd_max_fit_status, tq_device_status) */
+    TQ_ERR_DEVICE_CHECK = 8 /* a debug build's device-side index check failed (tq_device_status) */
 } tq_status;
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
@@ -56,7 +65,7 @@ typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
 /* packedDim (ops.ts, packedDim): bytes of one packed row of `dim` codes of
  * `bits` bits, dim*bits/8. Returns -TQ_ERR_ALIGNMENT when dim*bits is not a
  * multiple of 8 and -TQ_ERR_INVALID_ARG for dim < 0 or bits < 1. */
-int64_t tq_packed_dim(int64_t dim, int bits);
+TQ_API int64_t tq_packed_dim(int64_t dim, int bits);
 
 /* Encode (ops.ts: encodeKeys + packBits for K, encodeValues + packBits for V),
  * one fused kernel.
@@ -69,7 +78,7 @@ int64_t tq_packed_dim(int64_t dim, int bits);
  *               else is touched.
  * T == 0 (or B*H == 0) is a no-op that returns TQ_OK. B*H*T above
  * 2^31 - 1 - 2^24 rows returns TQ_ERR_INVALID_ARG (as for tq_decode_kv). */
-tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
+TQ_API tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
                        int64_t B, int64_t H, int64_t T, int64_t D,
                        int k_bits, int k_signed, int v_bits,
                        void* k_codes, void* k_scales, void* k_zeros,
@@ -82,7 +91,7 @@ tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtype,
  * k_out, v_out as contiguous [B,H,T,D] of type out_dtype. A key group whose
  * stored zero point is infinite (a constant group, see the ops.ts header)
  * decodes to NaN, as the page's formula (q + zero) * scale gives. */
-tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
+TQ_API tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_zeros,
                        const void* v_codes, const void* v_scales,
                        int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
                        int k_bits, int k_signed, int v_bits,
@@ -95,7 +104,7 @@ tq_status tq_decode_kv(const void* k_codes, const void* k_scales, const void* k_
  * rounded to out_dtype, with no inverse Hadamard transform and no signs.
  * Attention over V is linear in V, so a caller may attend over these values
  * and undo the rotation once per output row with tq_unrotate. */
-tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const void* k_zeros,
+TQ_API tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const void* k_zeros,
                                const void* v_codes, const void* v_scales,
                                int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap,
                                int k_bits, int k_signed, int v_bits,
@@ -109,14 +118,14 @@ tq_status tq_decode_kv_rotated(const void* k_codes, const void* k_scales, const 
  * aligned, [n_rows, D], and must not overlap (the input is read through
  * the read-only data path).
  * D in {64,128,256,512}; n_rows == 0 is a no-op; n_rows <= 2^31 - 1 - 2^24. */
-tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, void* out, void* stream);
+TQ_API tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, int64_t D, void* out, void* stream);
 
 /* Lloyd-Max index (ops.ts, searchsorted): idx[i] = number of boundaries of
  * the v_bits table strictly below u[i] (NaN -> 0), for n fp32 values already
  * in the rotated, RMS-normalised domain. u and idx are device pointers
  * (u 4-byte aligned, idx unaligned bytes). The same device routine the
  * encode kernel uses. */
-tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx, void* stream);
+TQ_API tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx, void* stream);
 
 /* Fused decode attention over a packed cache (ops.ts: the deferV branch of
  * tryDecodePackedKv, i.e. decodeKeys and decodeValuesRotated returning bf16,
@@ -151,7 +160,7 @@ tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8_t* idx
  * (else TQ_ERR_ALIGNMENT). B == 0 is a no-op. Two kernels are enqueued on
  * `stream`: the split pass, which cuts the (batch, kv head, 16-token tile)
  * space evenly over one wave of blocks, and the combine pass. */
-tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
+TQ_API tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
                               const void* k_codes, const void* k_scales, const void* k_zeros,
                               const void* v_codes, const void* v_scales,
                               int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
@@ -162,7 +171,7 @@ tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
 /* Bytes of scratch tq_decode_attention needs for these sizes on the current
  * device (the token chunking follows the device's SM count, so query it with
  * the same device current). Negative: -TQ_ERR_HEAD_DIM or -TQ_ERR_INVALID_ARG. */
-int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, int64_t D);
+TQ_API int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, int64_t D);
 
 /* tq_decode_attention for callers that cannot allocate device memory: no
  * counterpart on the pages (an interface addition of this library). Some
@@ -193,7 +202,7 @@ int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_t T, in
  *     stream or with events. Nothing in the array needs clearing between
  *     calls: each call writes every scratch record it reads. */
 #define TQ_ATTENTION_NOALLOC_SCRATCH_BYTES (64LL << 20)
-tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64_t Hq, int64_t Nq,
+TQ_API tq_status tq_decode_attention_noalloc(const void* q, int64_t B, int64_t Hq, int64_t Nq,
                                       const void* k_codes, const void* k_scales, const void* k_zeros,
                                       const void* v_codes, const void* v_scales,
                                       int64_t Hkv, int64_t T, int64_t D, int64_t t_cap,
@@ -235,7 +244,7 @@ typedef struct {
  * Sizes and descriptors are checked on the host (TQ_ERR_INVALID_ARG,
  * TQ_ERR_HEAD_DIM, TQ_ERR_BITS, TQ_ERR_ALIGNMENT) before anything is
  * enqueued; one kernel is enqueued per 48 destination rows. */
-tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H, int64_t D,
+TQ_API tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H, int64_t D,
                             int k_bits, int v_bits, void* k_codes, void* k_scales, void* k_zeros,
                             void* v_codes, void* v_scales, int64_t t_cap, int64_t width, void* stream);
 
@@ -258,7 +267,7 @@ tq_status tq_cache_assemble(const tq_row_source* rows, int64_t n_rows, int64_t H
  * grid barrier per iteration; if a wait gives up, centroids and boundaries
  * are left NaN and tq_lloyd_max_fit_status reports TQ_ERR_TIMEOUT);
  * n < 2^31. Returns once the work is enqueued. */
-tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
+TQ_API tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, const float* init,
                            float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
                            void* stream);
 
@@ -273,7 +282,7 @@ tq_status tq_lloyd_max_fit(const float* x, int64_t n, int levels, int iters, con
  *                 that died would; every other block's wait then runs out,
  *                 the error word is set and centroids and boundaries are
  *                 left NaN. Every wait stays bounded either way. */
-tq_status tq_lloyd_max_fit_bounded(const float* x, int64_t n, int levels, int iters, const float* init,
+TQ_API tq_status tq_lloyd_max_fit_bounded(const float* x, int64_t n, int levels, int iters, const float* init,
                                    float* centroids, float* boundaries, void* workspace, int64_t workspace_bytes,
                                    int64_t spin_limit, int absent_block, void* stream);
 
@@ -281,25 +290,32 @@ tq_status tq_lloyd_max_fit_bounded(const float* x, int64_t n, int levels, int it
  * then reads the fit's error word from the workspace (byte offset 8).
  * TQ_OK, or TQ_ERR_TIMEOUT when a block gave up at a grid barrier (the
  * results are then NaN); TQ_ERR_CUDA if the wait or the copy failed. */
-tq_status tq_lloyd_max_fit_status(const void* workspace, void* stream);
+TQ_API tq_status tq_lloyd_max_fit_status(const void* workspace, void* stream);
 
 /* Bytes of scratch tq_lloyd_max_fit needs (64 + 48 * levels), or
  * -TQ_ERR_INVALID_ARG for a level count that is not a power of two in
  * [2, 256]. */
-int64_t tq_lloyd_max_fit_workspace_size(int levels);
+TQ_API int64_t tq_lloyd_max_fit_workspace_size(int levels);
 
 /* Device-side failures of the library's kernels on the current device (no
  * counterpart on the pages: failure detection of this library). Kernels that
  * wait on an asynchronous copy (the decode's bulk-copy path) bound the wait;
  * one that gives up sets the device error word, stops early and leaves its
- * outputs incomplete. This call waits for `stream`, then returns TQ_OK, or
- * TQ_ERR_TIMEOUT once for each time the word was found set (it is cleared),
- * or TQ_ERR_CUDA if the wait or the copies failed. The first decode on a
- * device looks up the word's address (make it before any stream capture). */
-tq_status tq_device_status(void* stream);
+ * outputs incomplete. A debug build of the library (compiled with
+ * -DTQ_DEBUG_CHECKS) also checks the row and record indices of its kernels'
+ * global accesses against the buffers' extents, and an index outside them
+ * sets the word and skips the access (no trap). This call waits for
+ * `stream`, then returns TQ_OK; or TQ_ERR_DEVICE_CHECK (an index check
+ * failed) or TQ_ERR_TIMEOUT (a wait gave up), clearing the word; or
+ * TQ_ERR_CUDA if the wait or the copies failed. The first call of a kernel on
+ * a device looks up the word's address (make it before any stream capture). */
+TQ_API tq_status tq_device_status(void* stream);
+
+/* 1 in a debug build of the library (device-side index checks), else 0. */
+TQ_API int tq_debug_checks(void);
 
 /* Human-readable name of a status code (static string). */
-const char* tq_status_string(int status);
+TQ_API const char* tq_status_string(int status);
 
 #ifdef __cplusplus
 }

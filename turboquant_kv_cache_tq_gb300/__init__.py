@@ -34,7 +34,7 @@ GROUP = 32
 TQ_F32, TQ_BF16 = 0, 1
 _DTYPE = {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16}
 _NAMES = ("TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_HEAD_DIM", "TQ_ERR_BITS", "TQ_ERR_ALIGNMENT",
-          "TQ_ERR_DTYPE", "TQ_ERR_CUDA", "TQ_ERR_TIMEOUT")
+          "TQ_ERR_DTYPE", "TQ_ERR_CUDA", "TQ_ERR_TIMEOUT", "TQ_ERR_DEVICE_CHECK")
 
 _lock = threading.Lock()
 _lib = None
@@ -57,44 +57,52 @@ def lib() -> ctypes.CDLL:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
                     "libtq.so is not built (%s); run python -m turboquant_kv_cache_tq_gb300.build" % LIB_PATH)
-            L = ctypes.CDLL(LIB_PATH)
-            P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-            L.tq_packed_dim.restype = I64
-            L.tq_packed_dim.argtypes = [I64, I]
-            L.tq_encode_kv.restype = I
-            L.tq_encode_kv.argtypes = [P, P, I, I64, I64, I64, I64, I, I, I, P, P, P, P, P, I64, I64, P]
-            L.tq_decode_kv.restype = I
-            L.tq_decode_kv.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
-            L.tq_decode_kv_rotated.restype = I
-            L.tq_decode_kv_rotated.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
-            L.tq_unrotate.restype = I
-            L.tq_unrotate.argtypes = [P, I, I64, I64, P, P]
-            L.tq_lloyd_max_index.restype = I
-            L.tq_lloyd_max_index.argtypes = [P, I64, I, P, P]
-            L.tq_decode_attention.restype = I
-            L.tq_decode_attention.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P,
-                                              ctypes.c_float, P, I, P, I64, P]
-            L.tq_decode_attention_noalloc.restype = I
-            L.tq_decode_attention_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I,
-                                                      I, P, ctypes.c_float, P, I, P]
-            L.tq_decode_attention_workspace_size.restype = I64
-            L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
-            L.tq_cache_assemble.restype = I
-            L.tq_cache_assemble.argtypes = [P, I64, I64, I64, I, I, P, P, P, P, P, I64, I64, P]
-            L.tq_lloyd_max_fit.restype = I
-            L.tq_lloyd_max_fit.argtypes = [P, I64, I, I, P, P, P, P, I64, P]
-            L.tq_lloyd_max_fit_bounded.restype = I
-            L.tq_lloyd_max_fit_bounded.argtypes = [P, I64, I, I, P, P, P, P, I64, I64, I, P]
-            L.tq_lloyd_max_fit_status.restype = I
-            L.tq_lloyd_max_fit_status.argtypes = [P, P]
-            L.tq_lloyd_max_fit_workspace_size.restype = I64
-            L.tq_lloyd_max_fit_workspace_size.argtypes = [I]
-            L.tq_device_status.restype = I
-            L.tq_device_status.argtypes = [P]
-            L.tq_status_string.restype = ctypes.c_char_p
-            L.tq_status_string.argtypes = [I]
-            _lib = L
+            _lib = load_library(LIB_PATH)
     return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """A build of the C ABI at `path` (libtq.so or its debug variant
+    libtq_debug.so) with every entry point's argument types declared."""
+    L = ctypes.CDLL(path)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    L.tq_packed_dim.restype = I64
+    L.tq_packed_dim.argtypes = [I64, I]
+    L.tq_encode_kv.restype = I
+    L.tq_encode_kv.argtypes = [P, P, I, I64, I64, I64, I64, I, I, I, P, P, P, P, P, I64, I64, P]
+    L.tq_decode_kv.restype = I
+    L.tq_decode_kv.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
+    L.tq_decode_kv_rotated.restype = I
+    L.tq_decode_kv_rotated.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, P, P, I, P]
+    L.tq_unrotate.restype = I
+    L.tq_unrotate.argtypes = [P, I, I64, I64, P, P]
+    L.tq_lloyd_max_index.restype = I
+    L.tq_lloyd_max_index.argtypes = [P, I64, I, P, P]
+    L.tq_decode_attention.restype = I
+    L.tq_decode_attention.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P,
+                                      ctypes.c_float, P, I, P, I64, P]
+    L.tq_decode_attention_noalloc.restype = I
+    L.tq_decode_attention_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P, P, I64, I64, I64, I64, I, I,
+                                              I, P, ctypes.c_float, P, I, P]
+    L.tq_decode_attention_workspace_size.restype = I64
+    L.tq_decode_attention_workspace_size.argtypes = [I64, I64, I64, I64]
+    L.tq_cache_assemble.restype = I
+    L.tq_cache_assemble.argtypes = [P, I64, I64, I64, I, I, P, P, P, P, P, I64, I64, P]
+    L.tq_lloyd_max_fit.restype = I
+    L.tq_lloyd_max_fit.argtypes = [P, I64, I, I, P, P, P, P, I64, P]
+    L.tq_lloyd_max_fit_bounded.restype = I
+    L.tq_lloyd_max_fit_bounded.argtypes = [P, I64, I, I, P, P, P, P, I64, I64, I, P]
+    L.tq_lloyd_max_fit_status.restype = I
+    L.tq_lloyd_max_fit_status.argtypes = [P, P]
+    L.tq_lloyd_max_fit_workspace_size.restype = I64
+    L.tq_lloyd_max_fit_workspace_size.argtypes = [I]
+    L.tq_device_status.restype = I
+    L.tq_device_status.argtypes = [P]
+    L.tq_debug_checks.restype = I
+    L.tq_debug_checks.argtypes = []
+    L.tq_status_string.restype = ctypes.c_char_p
+    L.tq_status_string.argtypes = [I]
+    return L
 
 
 def tq_status_string(status: int) -> str:

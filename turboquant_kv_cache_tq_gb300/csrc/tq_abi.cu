@@ -163,6 +163,8 @@ extern "C" tq_status tq_encode_kv(const void* k, const void* v, tq_dtype in_dtyp
   p.rot_scale = rotation_scale(D);
   p.tdiv = make_fast_div(static_cast<int>(T));
   p.neg_zero = -0.0f;
+  p.cache_rows = B * H * t_cap;
+  p.err = device_error_word();
   const bool bf16 = in_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -211,6 +213,7 @@ tq_status decode_impl(const void* k_codes, const void* k_scales, const void* k_z
   p.tdiv = make_fast_div(static_cast<int>(T));
   p.neg_zero = -0.0f;
   p.err = device_error_word();
+  p.cache_rows = B * H * t_cap;
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -257,6 +260,7 @@ extern "C" tq_status tq_unrotate(const void* x, tq_dtype dtype, int64_t n_rows, 
   p.out = out;
   p.rows = static_cast<int>(n_rows);
   p.rot_scale = rotation_scale(D);
+  p.err = device_error_word();
   const bool bf16 = dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -353,6 +357,9 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   p.total_tiles = bhkv * tiles_per_bh;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rot_scale = rotation_scale(D);
+  p.cache_rows = bhkv * t_cap;
+  p.ws_records = workspace_bytes / (kAttnRecordFloats(D) * 4);
+  p.err = device_error_word();
   const int kmode = key_mode(k_bits, k_signed);
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -376,9 +383,17 @@ extern "C" tq_status tq_device_status(void* stream) {
   if (v != 0) {
     const unsigned zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ERR_CUDA;
-    return TQ_ERR_TIMEOUT;
+    return (v & kErrIndex) ? TQ_ERR_DEVICE_CHECK : TQ_ERR_TIMEOUT;
   }
   return TQ_OK;
+}
+
+extern "C" int tq_debug_checks(void) {
+#ifdef TQ_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 extern "C" const char* tq_status_string(int status) {
@@ -391,6 +406,7 @@ extern "C" const char* tq_status_string(int status) {
     case TQ_ERR_DTYPE: return "TQ_ERR_DTYPE: dtype must be TQ_F32 or TQ_BF16";
     case TQ_ERR_CUDA: return "TQ_ERR_CUDA: the CUDA runtime reported an error";
     case TQ_ERR_TIMEOUT: return "TQ_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case TQ_ERR_DEVICE_CHECK: return "TQ_ERR_DEVICE_CHECK: a debug build's device-side index check failed";
     default: return "unknown tq_status";
   }
 }

@@ -323,8 +323,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     // half of each row when SPL = 2); every step commits one copy group
     // (empty past the end).
     auto issue = [&](int k) {
-      if (k < my_tiles) {
-        const long long t = tok0 + static_cast<long long>(team + k * kTeams) * kAttnTile;
+      const long long tk = tok0 + static_cast<long long>(team + k * kTeams) * kAttnTile;
+      if (k < my_tiles && TQ_CHECK(tk >= 0 && tk + kAttnTile <= static_cast<long long>(bh + 1) * p.t_cap, p.err)) {
+        const long long t = tk;
         const uint32_t dst = ring_sh + (k % S) * L::STAGE;
         if constexpr (SPL == 1) {
           copy_region<kAttnTile * L::PDK>(dst + L::KC, p.k_codes + t * L::PDK, lane);
@@ -606,6 +607,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
     }
     __syncthreads();
     const float* all = reinterpret_cast<const float*>(s_work);
+    if (!TQ_CHECK(static_cast<long long>(blockIdx.x) + bh < p.ws_records, p.err)) continue;
     float* rec = p.ws + (static_cast<long long>(blockIdx.x) + bh) * SM::REC;
     for (int i = threadIdx.x; i < Rq * D; i += blockDim.x) {
       const int r = i / D;
@@ -682,6 +684,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnPa
     c0 = static_cast<int>(((x0 + 1) * p.grid - 1) / p.total_tiles);
     n_rec = static_cast<int>(((x1 + 1) * p.grid - 1) / p.total_tiles) - c0 + 1;
   }
+  if (!TQ_CHECK(static_cast<long long>(c0) + bh + n_rec <= p.ws_records, p.err)) n_rec = 0;
   const float* recs = p.ws + (static_cast<long long>(c0) + bh) * REC;
   float mx = kNegInf;
   for (int s = warp; s < n_rec; s += NW) mx = fmaxf(mx, recs[s * REC + r]);

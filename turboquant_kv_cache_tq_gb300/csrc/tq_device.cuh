@@ -80,6 +80,13 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) { return fma2(b, f2(-
 // RN(a * b) that cannot be fused into a consumer; nz must hold a runtime -0.0
 __device__ __forceinline__ float2 mul0(float2 a, float2 b, float2 nz) { return fma2(a, b, nz); }
 
+// A debug build's index check (TQ_CHECK): records a failure in the device
+// error word and returns whether the access may go ahead.
+__device__ __forceinline__ bool debug_check(bool ok, unsigned* err) {
+  if (!ok && err != nullptr) atomicOr(err, kErrIndex);
+  return ok;
+}
+
 // min / max that return NaN when either operand is NaN (PTX min.NaN / max.NaN).
 __device__ __forceinline__ float fmin_nan(float a, float b) {
   float d;

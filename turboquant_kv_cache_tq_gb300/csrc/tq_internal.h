@@ -13,6 +13,19 @@ struct FastDiv {
   int shift;
 };
 
+// Bits of the library's device error word (see device_error_word).
+constexpr unsigned kErrTimeout = 1u;  // a bounded wait gave up
+constexpr unsigned kErrIndex = 2u;    // a debug build's index check failed
+
+// Device-side index checks of a debug build (-DTQ_DEBUG_CHECKS): TQ_CHECK(ok,
+// err) is `ok`, and a false `ok` also sets kErrIndex in *err; the caller
+// skips the access. In a normal build it is `true` and compiles to nothing.
+#ifdef TQ_DEBUG_CHECKS
+#define TQ_CHECK(ok, err) (::tq::debug_check((ok), (err)))
+#else
+#define TQ_CHECK(ok, err) true
+#endif
+
 // Key modes: (bits, signed) pairs the key path supports.
 enum KeyMode : int { kK2 = 0, kK4 = 1, kK5 = 2, kK8 = 3, kK8Signed = 4 };
 
@@ -32,6 +45,8 @@ struct EncodeParams {
   float rot_scale;      // fp32(1/sqrt(D))
   FastDiv tdiv;         // division by T
   float neg_zero;       // -0.0f (a runtime value, see mul0)
+  long long cache_rows; // B*H*t_cap (debug checks)
+  unsigned* err;        // the library's device error word, or null
 };
 
 struct DecodeParams {
@@ -51,7 +66,8 @@ struct DecodeParams {
   float neg_zero;       // -0.0f
   int pdk, pdv;         // bytes of a packed K / V row
   int ng;               // groups per row (D / 32)
-  unsigned* err;        // the library's device error word (bit 0: a bounded wait gave up), or null
+  unsigned* err;        // the library's device error word, or null
+  long long cache_rows; // B*H*t_cap (debug checks)
 };
 
 struct UnrotateParams {
@@ -59,6 +75,7 @@ struct UnrotateParams {
   void* out;            // [rows, D] same type
   int rows;
   float rot_scale;
+  unsigned* err;        // the library's device error word, or null
 };
 
 // Fused decode attention: at most 16 query rows per kv head (Hq/Hkv heads
@@ -87,6 +104,9 @@ struct AttnParams {
   int grid;             // split blocks (set by the launcher)
   float scale_log2;     // softmax scale * log2(e)
   float rot_scale;      // fp32(1/sqrt(D))
+  long long cache_rows; // B * Hkv * t_cap (debug checks)
+  long long ws_records; // records the workspace holds (debug checks)
+  unsigned* err;        // the library's device error word, or null
 };
 
 // Launchers per head_dim, one translation unit per input or output type (and

@@ -493,8 +493,10 @@ __global__ void __launch_bounds__(EncodeShape<D, VB, F32, ALLOW_REP>::kBlockThre
       const char* src = static_cast<const char*>(ord.is_v(it, k) ? p.v : p.k) +
                         (static_cast<size_t>(r) * D + kGroup * l) * (F32 ? 4 : 2);
       const uint32_t dst = lane_ring_sh + (k & (R::kStages - 1)) * R::kStageBytes;
+      if (TQ_CHECK(r >= 0 && r < p.rows, p.err)) {
 #pragma unroll
-      for (int j = 0; j < R::kChunks; ++j) cp_async16(dst + 16 * (j ^ swz), src + 16 * j);
+        for (int j = 0; j < R::kChunks; ++j) cp_async16(dst + 16 * (j ^ swz), src + 16 * j);
+      }
     }
     cp_async_commit();
   };
@@ -530,11 +532,12 @@ __global__ void __launch_bounds__(EncodeShape<D, VB, F32, ALLOW_REP>::kBlockThre
     const int r = valid ? r0 : p.rows - 1;
     const int bh = fast_div(r, p.tdiv);
     const long long orow = static_cast<long long>(bh) * p.t_cap + p.t_off + (r - bh * p.T);
+    const bool store = valid && TQ_CHECK(orow >= 0 && orow < p.cache_rows, p.err);
     if (!ord.is_v(it, k)) {
-      encode_key_item<KMODE, F32>(in, p.neg_zero, valid, p.k_codes + orow * pdk + 4 * M::B * l,
+      encode_key_item<KMODE, F32>(in, p.neg_zero, store, p.k_codes + orow * pdk + 4 * M::B * l,
                                   p.k_scales + orow * NG + l, p.k_zeros + orow * NG + l, no_prefetch);
     } else {
-      encode_value_item<G::LPR, VB, F32, SH::REP, kRegSigns>(in, l, signs, cells, rep_bias, p.rot_scale, p.neg_zero, valid,
+      encode_value_item<G::LPR, VB, F32, SH::REP, kRegSigns>(in, l, signs, cells, rep_bias, p.rot_scale, p.neg_zero, store,
                                          p.v_codes + orow * pdv + 4 * VB * l, p.v_scales + orow * NG + l,
                                          no_prefetch);
     }
@@ -555,6 +558,12 @@ template <int KB, int VB>
 __device__ __forceinline__ void load_packed_item(const DecodeParams& p, bool is_v, long long irow, int l,
                                                  PackedIn<(KB > VB ? KB : VB)>& in) {
   constexpr int W = KB > VB ? KB : VB;
+  if (!TQ_CHECK(irow >= 0 && irow < p.cache_rows, p.err)) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) in.w[k] = 0u;
+    in.sz = 0u;
+    return;
+  }
   if (is_v) {
     uint32_t t[VB];
     load_words<VB>(p.v_codes + irow * p.pdv + 4 * VB * l, t);
@@ -793,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(Deco
   for (int it = gw; it < items; it += n_warps, ++step) {
     const bool is_v = ((it ^ step) & 1) != 0;
     const int r0 = (it >> 1) * G::RPW + sub;
-    const bool valid = r0 < p.rows;
+    const bool valid = r0 < p.rows && TQ_CHECK(r0 >= 0, p.err);
     const int r = valid ? r0 : p.rows - 1;
     const size_t out_off = static_cast<size_t>(r) * D + kGroup * l;
 
@@ -984,7 +993,7 @@ __global__ void __launch_bounds__(kThreads) unrotate_kernel(UnrotateParams p) {
   load_sign_words(s_sign, l, S);
   for (int tile = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < tiles; tile += n_warps) {
     const int r0 = tile * G::RPW + sub;
-    const bool valid = r0 < p.rows;
+    const bool valid = r0 < p.rows && TQ_CHECK(r0 >= 0, p.err);
     const size_t off = static_cast<size_t>(valid ? r0 : p.rows - 1) * D + kGroup * l;
     ItemIn<F32> in;
     load_item<F32>(p.x, off, in);
