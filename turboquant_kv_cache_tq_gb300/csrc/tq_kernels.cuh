@@ -12,11 +12,12 @@
 //   centroid * scale, Hadamard transform, signs for V (decodeValues).
 //
 // Division-free quantisation:
-//   K: RN(x / se) is obtained exactly from the reciprocal by one correction
-//      step (q0 = RN(x * RN(1/se)), r = x - q0 * se exact, q = RN(q0 + r *
-//      RN(1/se))), then RN(q - zp) and rint, the page's operations in order,
-//      so K codes are exactly the page's. A warp with a group whose codes
-//      need the clamp (or whose quotient could overflow) takes IEEE division.
+//   K: RN(x / se) is obtained exactly from the reciprocal by one remainder
+//      correction (div_by_recip: q0 = RN(x y), q = RN(q0 + RN(x - q0 se) y),
+//      y = RN(1/se); correctly rounded, see there), then RN(q - zp) and rint,
+//      the page's operations in order, so K codes are exactly the page's. A
+//      warp with a group whose codes need the clamp (or whose quotient could
+//      overflow) takes IEEE division.
 //   V: the index is count(boundaries < v) for the exact product
 //      v = y * RN(1/se), which is within one ulp of RN(y / se) (|v| <=
 //      sqrt(32), so within 5e-7); it can only differ from the divided value's
@@ -215,6 +216,28 @@ struct KeySpec {
   static constexpr int kHi = kMax;
 };
 
+// RN(a / b) from y = RN(1 / b) without a division: q0 = RN(a y), then one
+// remainder correction q = RN(q0 + RN(a - b q0) y) (two fmas). Why q is the
+// correctly rounded quotient (the argument is scale-free; Bi is b's 24-bit
+// integer significand, "ulp" the spacing of a / b's fp32 grid):
+// y = (1 + e) / b with |e| <= Bi 2^-48 < 2^-24, so q0 is within 1.5 ulp of
+// a / b and the corrected value before its rounding, z, within 3 2^-24 ulp.
+// q can only be wrong if a rounding midpoint m lies between z and a / b, so
+// within d <= 3 2^-24 ulp of a / b. Then |a y - m| < 1 ulp (|m e| < 1 ulp,
+// and only when M Bi >= 2^49 - 3 2^25, for m's 25-bit odd significand M, does
+// it come within d of one ulp; no quotient lies that close to a midpoint in
+// that corner, checked exhaustively on the host), so q0 = m +- ulp / 2 is
+// within one ulp of a / b, the remainder a - b q0 is exact (Markstein) and
+// z - a / b = -e (q0 - a / b), of magnitude below |e| (ulp / 2 + d). As
+// a - m b is a nonzero multiple of ulp(b) ulp / 2, d >= ulp / (2 Bi), and
+// |e| (Bi + 1) < 1 (Bi (Bi + 1) < 2^48): so |z - a / b| < d and z stays on
+// a / b's side of m. Needs a / b and the remainder representable without
+// overflow or underflow.
+__device__ __forceinline__ float div_by_recip(float a, float b, float y) {
+  const float q0 = __fmul_rn(a, y);
+  return __fmaf_rn(__fmaf_rn(-q0, b, a), y, q0);
+}
+
 // Exact per-element quantisation (the page's operations, IEEE division).
 template <int KMODE>
 __device__ __forceinline__ uint32_t key_code_exact(float x, float se, float zp) {
@@ -305,18 +328,16 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
   prefetch();
   if (mn == 0.0f || mx == 0.0f) scan_min_max(X, mn, mx);
 
-  // The group's quotients by the reciprocal and one remainder correction
-  // (see code_bits below). scale = RN(range / levels): exact for every finite
-  // range >= 2^-100 (checked exhaustively on the host for all five level
-  // counts); below that it can be an ulp off, which changes neither
-  // RN(scale + eps) (= eps) nor the fp16 scale (0). Inf and NaN ranges keep
-  // IEEE semantics through the plain product.
+  // The group's quotients from the reciprocal with one remainder correction
+  // (div_by_recip; code_bits below for the elements). scale = RN(range /
+  // levels); a range below 2^-100 could make the remainder underflow, which
+  // changes neither RN(scale + eps) (= eps) nor the fp16 scale (0). Inf and
+  // NaN ranges keep IEEE semantics through the plain product.
   constexpr float kLevels = static_cast<float>(M::SIGNED ? 2 * M::kMax : M::kMax);
   constexpr float kInvLevels = 1.0f / kLevels;
   const float range = __fsub_rn(mx, mn);
-  const float sq0 = __fmul_rn(range, kInvLevels);
   const float scale =
-      range <= 3.402823466e38f ? __fmaf_rn(__fmaf_rn(-sq0, kLevels, range), kInvLevels, sq0) : sq0;
+      range <= 3.402823466e38f ? div_by_recip(range, kLevels, kInvLevels) : __fmul_rn(range, kInvLevels);
   const float se = __fadd_rn(scale, kEps);
   const float inv = __frcp_rn(se);
   // zero point: RN(mn / se), or RN((mx + mn) / (2 se)) = RN((mx + mn) / se) / 2
@@ -330,23 +351,20 @@ __device__ __forceinline__ void encode_key_item(ItemIn<F32>& in, float neg_zero,
   const float zq0 = __fmul_rn(num, inv);
   float zq;
   if (fabsf(zq0) <= 3.402823466e38f && range <= 3.402823466e38f) {
-    zq = copysignf(__fmaf_rn(__fmaf_rn(-zq0, se, num), inv, zq0), num);
+    zq = copysignf(div_by_recip(num, se, inv), num);
     if constexpr (M::SIGNED) zq = __fmul_rn(zq, 0.5f);
   } else {
     zq = M::SIGNED ? __fdiv_rn(num, __fmul_rn(2.0f, se)) : __fdiv_rn(num, se);
   }
   const float zp = rintf(zq);
   const float2 nz = f2(neg_zero);
-  // Code of a pair as the float bit pattern kMagicBits + rint(RN(RN(x/se) - zp)).
-  // RN(x/se) exactly by one correction step: with inv = RN(1/se) and
-  // q0 = RN(x * inv) (within an ulp of x/se), the remainder r = x - q0 * se is
-  // exact and RN(q0 + r * inv) is the correctly rounded quotient, barring
-  // overflow of x/se (the caller's range test rejects it) and underflow of r
-  // (only when |x/se| < 2^-70, too small to move rint(q - zp)).
+  // Code of a pair as the float bit pattern kMagicBits + rint(RN(RN(x/se) - zp)),
+  // RN(x/se) by div_by_recip's correction in packed form, barring overflow
+  // of x/se (the caller's range test rejects it) and underflow of the
+  // remainder (only when |x/se| < 2^-70, too small to move rint(q - zp)).
   auto code_bits = [&](float2 x) {
     const float2 q0 = mul0(x, f2(inv), nz);  // rounded: it is the quotient's first guess
-    const float2 r = fma2(q0, f2(-se), x);
-    const float2 q = fma2(r, f2(inv), q0);
+    const float2 q = fma2(fma2(q0, f2(-se), x), f2(inv), q0);
     return add2(add2(q, f2(-zp)), f2(kMagic));  // RN(q - zp), then rint
   };
   const int lo_bits = static_cast<int>(kMagicBits) + M::kLo;
