@@ -19,9 +19,13 @@
  *       v_codes  X = tq_packed_dim(D, v_bits) bytes, v_scales X = D/32 fp16.
  *     Rows (b, h, t) are packed independently, so a token is a whole row of
  *     each buffer and appends never touch another token's bytes.
- *   - All buffer pointers are device pointers owned by the caller; the library
- *     never allocates, frees or keeps them. Every buffer pointer must be 16-byte
- *     aligned.
+ *   - All buffer pointers are device-accessible pointers owned by the caller
+ *     (device memory, or pinned host memory mapped into the device's address
+ *     space, which the kernels then read or write over the CPU-GPU link); the
+ *     library never allocates, frees or keeps them. Every buffer pointer must
+ *     be 16-byte aligned. A decode whose buffers are all device memory moves
+ *     its data with bulk asynchronous copies; one with a buffer in host memory
+ *     takes per-thread loads and stores.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and runs asynchronously; the call returns once it is enqueued.
  *   - Arguments are checked on the host before anything is launched; a

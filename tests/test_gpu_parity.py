@@ -459,3 +459,32 @@ def test_non_finite_rows_match_oracle(D, vb, dtype, T):
     k, v = _non_finite_kv(1, 1, T, D, dtype, 900 + D + vb + T, 60)
     for kb, ks in ((8, True), (4, False)):
         check_roundtrip(k, v, kb, ks, vb)
+
+
+# ---- buffers in pinned host memory (read and written over the CPU-GPU link) ------------
+@pytest.mark.parametrize("D,vb", [(128, 8), (128, 3), (512, 5)])
+def test_pinned_host_buffers(D, vb):
+    """K, V read straight from pinned host memory and decoded outputs written
+    straight to pinned host memory give the same bytes as device buffers
+    (a decode with a host buffer takes the per-lane kernel, not bulk
+    copies)."""
+    rpw = 32 // (D // 32)
+    k = _rand((2, 4, 16 * rpw, D), torch.bfloat16, 70 + D + vb)
+    v = _rand((2, 4, 16 * rpw, D), torch.bfloat16, 71 + D + vb)
+    kh, vh = k.pin_memory(), v.pin_memory()
+    B, H, T, _ = k.shape
+    c_dev = gpu_encode(k, v, 8, True, vb)
+    c_host = tq.alloc_cache(B, H, T, D, 8, vb)
+    s = torch.cuda.current_stream()
+    tq.tq_encode_kv(kh, vh, 8, True, vb, c_host, stream=s)
+    torch.cuda.synchronize()
+    a, b = cache_to_numpy(c_dev), cache_to_numpy(c_host)
+    for n in a:
+        assert np.array_equal(a[n], b[n]), n
+    for dt in (torch.bfloat16, torch.float32):
+        kd, vd = tq.tq_decode_kv(c_dev, T, 8, True, vb, out_dtype=dt)
+        ko = torch.empty((B, H, T, D), dtype=dt).pin_memory()
+        vo = torch.empty((B, H, T, D), dtype=dt).pin_memory()
+        tq.tq_decode_kv(c_dev, T, 8, True, vb, out_dtype=dt, k_out=ko, v_out=vo, stream=s)
+        torch.cuda.synchronize()
+        assert torch.equal(kd.cpu(), ko) and torch.equal(vd.cpu(), vo)

@@ -95,6 +95,21 @@ int key_mode(int bits, int is_signed) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether every pointer is device memory (as opposed to pinned host memory
+// mapped into the device's address space, managed or unregistered memory).
+// Bulk asynchronous copies are only used between device and shared memory.
+bool all_device_memory(const void* const* ptrs, int n) {
+  for (int i = 0; i < n; ++i) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+      cudaGetLastError();  // leave no sticky error behind
+      return false;
+    }
+    if (a.type != cudaMemoryTypeDevice) return false;
+  }
+  return true;
+}
+
 // Shared checks of encode and decode; fills rows.
 tq_status check_common(int64_t B, int64_t H, int64_t T, int64_t D, int64_t t_cap, int64_t t_off,
                        int k_bits, int k_signed, int v_bits, int dtype, long long* rows) {
@@ -214,6 +229,7 @@ tq_status decode_impl(const void* k_codes, const void* k_scales, const void* k_z
   p.neg_zero = -0.0f;
   p.err = device_error_word();
   p.cache_rows = B * H * t_cap;
+  p.device_memory = out_dtype == TQ_BF16 && all_device_memory(ptrs, 7) ? 1 : 0;
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -47,6 +47,10 @@
 namespace tq {
 
 constexpr int kAttnWarps = 4;
+#ifndef TQ_ATTN_MIN_TEAM_TILES
+#define TQ_ATTN_MIN_TEAM_TILES 8
+#endif
+constexpr long long kAttnMinTeamTiles = TQ_ATTN_MIN_TEAM_TILES;
 constexpr int kAttnThreads = 32 * kAttnWarps;
 constexpr int kAttnTile = 16;  // tokens per warp step
 constexpr int kAttnRows = kAttnMaxRows;  // query rows per kv head (M of the score MMA)
@@ -777,6 +781,12 @@ cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
   // one wave of resident blocks (at most kAttnGridPerSm per SM, the bound
   // the workspace is sized for), never more blocks than tiles
   long long grid = static_cast<long long>(per_sm < kAttnGridPerSm ? per_sm : kAttnGridPerSm) * sm_count();
+  // each team of warps gets at least kAttnMinTeamTiles tiles, so the per-block
+  // start (value table, query operands) and the record merge stay small next
+  // to its work when few heads hold many tiles
+  const long long teams = kAttnWarps / AttnSplit<D>::SPL;
+  const long long by_work = (p.total_tiles + teams * kAttnMinTeamTiles - 1) / (teams * kAttnMinTeamTiles);
+  if (grid > by_work) grid = by_work;
   if (grid > p.total_tiles) grid = p.total_tiles;
   if (grid < 1) grid = 1;
   p.grid = static_cast<int>(grid);

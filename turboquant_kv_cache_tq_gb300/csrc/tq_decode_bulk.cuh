@@ -21,9 +21,10 @@
 // interleaved order (item gw + k n, a V item when (item ^ k) is odd).
 //
 // Used when every tile's rows are contiguous and 16-byte aligned in all five
-// packed buffers and the outputs are bf16 (the host checks it: T a multiple
-// of RPW, t_cap times each packed row size a multiple of 16); other launches
-// take the per-lane kernel.
+// packed buffers, the outputs are bf16 and every buffer is device memory
+// (the host checks it: T a multiple of RPW, t_cap times each packed row size
+// a multiple of 16, the pointers' memory type); other launches, for instance
+// outputs written straight to pinned host memory, take the per-lane kernel.
 //
 // Waits on the mbarriers are bounded: a wait that gives up sets bit 0 of the
 // library's device error word, waits (bounded) for the copies the warp still
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
 // 16-byte aligned base pointers).
 template <int D>
 inline bool bulk_decode_ok(const DecodeParams& p, bool out_bf16) {
-  if (!out_bf16 || p.T % Geo<D>::RPW != 0) return false;
+  if (!out_bf16 || !p.device_memory || p.T % Geo<D>::RPW != 0) return false;
   const long long row_bytes[] = {p.pdk, p.pdv, 2LL * p.ng};
   for (long long x : row_bytes)
     if ((p.t_cap * x) % 16 != 0) return false;

@@ -68,6 +68,7 @@ struct DecodeParams {
   int ng;               // groups per row (D / 32)
   unsigned* err;        // the library's device error word, or null
   long long cache_rows; // B*H*t_cap (debug checks)
+  int device_memory;    // every buffer is device memory (bulk copies allowed)
 };
 
 struct UnrotateParams {
