@@ -691,6 +691,27 @@ def copy_floor(dev, reps: int):
     e1.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps / 32
     print("copy floor (32 x 11.67 MB copies in a CUDA graph): %.2f us per launch, %.0f GB/s" % (us, 23330816 / us / 1e3))
+    # the launch floor: 32 launches of a one-element kernel in a CUDA graph
+    tiny = [torch.zeros(1, device=dev) for _ in range(32)]
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for t in tiny:
+            t.add_(1.0)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(g2, stream=s):
+        for t in tiny:
+            t.add_(1.0)
+    for _ in range(10):
+        g2.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            g2.replay()
+    e1.record(s)
+    e1.synchronize()
+    print("launch floor (32 one-element kernels in a CUDA graph): %.2f us per launch"
+          % (1e3 * e0.elapsed_time(e1) / reps / 32))
 
 
 def host_link_floor(dev, reps: int):

@@ -488,3 +488,16 @@ def test_pinned_host_buffers(D, vb):
         tq.tq_decode_kv(c_dev, T, 8, True, vb, out_dtype=dt, k_out=ko, v_out=vo, stream=s)
         torch.cuda.synchronize()
         assert torch.equal(kd.cpu(), ko) and torch.equal(vd.cpu(), vo)
+
+
+@pytest.mark.parametrize("D", [256, 512])
+@pytest.mark.parametrize("vb", [2, 3, 4, 5, 8])
+def test_wide_encode_every_row(D, vb):
+    """bf16 launches of at least 65536 rows take the wide encode shape (cell
+    tables replicated per lane, 512-thread blocks); at head_dim 256 and 512 a
+    row spans 8 and 16 lanes (3 and 4 cross-lane Hadamard stages). Every row
+    against the oracle at every width, with a ragged last tile."""
+    T = 65536 + 2 * (32 // (D // 32)) + 1
+    k = _rand((1, 1, T, D), torch.bfloat16, 40 + D + vb)
+    v = _rand((1, 1, T, D), torch.bfloat16, 41 + D + vb, scale=2.0)
+    check_roundtrip(k, v, 8, True, vb)
