@@ -46,12 +46,10 @@
 
 namespace tq {
 
-constexpr int kAttnWarps = 4;
 #ifndef TQ_ATTN_MIN_TEAM_TILES
 #define TQ_ATTN_MIN_TEAM_TILES 8
 #endif
 constexpr long long kAttnMinTeamTiles = TQ_ATTN_MIN_TEAM_TILES;
-constexpr int kAttnThreads = 32 * kAttnWarps;
 constexpr int kAttnTile = 16;  // tokens per warp step
 constexpr int kAttnRows = kAttnMaxRows;  // query rows per kv head (M of the score MMA)
 
@@ -62,7 +60,6 @@ struct AttnLayout {
   static constexpr int NG = D / kGroup;
   static constexpr int PDK = D * KB / 8;
   static constexpr int PDV = D * VB / 8;
-  static constexpr int STAGES = D >= 256 ? 2 : 3;
   // one stage: the tile's rows of the five packed buffers, back to back
   static constexpr int KC = 0;                        // K codes  [16][PDK]
   static constexpr int KS = KC + kAttnTile * PDK;     // K scales [16][NG] fp16
@@ -74,7 +71,6 @@ struct AttnLayout {
   // value lookup table (see ValueTable): pairs of centroids for widths up to
   // 4 bits, once per half-warp lane; single centroids once per lane above
   static constexpr int CENT = VB <= 4 ? (16 * 8) << (2 * VB) : (32 * 4) << VB;
-  static constexpr int RING = kAttnWarps * STAGES * STAGE;
   // per-lane element ranges
   static constexpr int EK = D / 4;  // keys: token g, elements [c EK, (c+1) EK)
   static constexpr int EV = D / 8;  // values: elements [g EV, (g+1) EV) of four tokens
@@ -97,21 +93,42 @@ struct AttnSplit {
   static constexpr int DH = D / SPL;
 };
 
+// Warps per block (NW) and ring stages per warp (S). A block's warps share
+// its value table; the 32 KB tables (4-bit pairs, 8-bit singles) would hold
+// a four-warp block of head_dim <= 128 to two or three blocks per SM (8 or 12
+// warps), so those blocks take eight warps with two stages each: two blocks,
+// 16 warps per SM, the register limit at 128 registers a thread.
+template <int D, int VB, int NT>
+struct AttnShape {
+  static constexpr int DH = AttnSplit<D>::DH;
+  static constexpr int CENT = VB <= 4 ? (16 * 8) << (2 * VB) : (32 * 4) << VB;
+  static constexpr bool WIDE = DH <= 128 && CENT >= 32768 && NT == 1;
+  static constexpr int NW = WIDE ? 8 : 4;
+  static constexpr int THREADS = 32 * NW;
+  static constexpr int S = (WIDE || DH >= 256) ? 2 : 3;
+  static constexpr int MIN_BLOCKS = WIDE ? 2 : 0;  // 0: no bound (the compiler's choice)
+};
+
 // Block-level shared memory of the split kernel over the per-warp layout L:
 // value table | score exchange (SPL = 2) | ring of stages, later the merge
 // area of one record per warp group.
 template <int D, int KB, int VB, int NT>
 struct AttnSmem {
   using L = AttnLayout<AttnSplit<D>::DH, KB, VB>;
+  using Shape = AttnShape<D, VB, NT>;
+  static_assert(Shape::CENT == L::CENT, "one table size");
+  static constexpr int NW = Shape::NW;
+  static constexpr int S = Shape::S;
+  static constexpr int RING = NW * S * L::STAGE;
   static constexpr int SPL = AttnSplit<D>::SPL;
   static constexpr int REC = kAttnRows * (D + 2);  // floats of a partial record: m[16], l[16], O[16][D]
   static_assert(REC == kAttnRecordFloats(D), "record layout shared with the host");
-  static constexpr int MERGE = (kAttnWarps / SPL) * REC * 4;
+  static constexpr int MERGE = (NW / SPL) * REC * 4;
   // two slots (tile parity) x warps x 32 lanes x NT x 4 partial scores
-  static constexpr int XCHG = SPL > 1 ? 2 * kAttnWarps * 32 * NT * 4 * 4 : 0;
+  static constexpr int XCHG = SPL > 1 ? 2 * NW * 32 * NT * 4 * 4 : 0;
   static constexpr int XOFF = L::CENT;
   static constexpr int WORK = XOFF + XCHG;
-  static constexpr int SMEM = WORK + (L::RING > MERGE ? L::RING : MERGE);
+  static constexpr int SMEM = WORK + (RING > MERGE ? RING : MERGE);
 };
 
 // Copy ROWS rows of HB bytes (a multiple of 16) taken at a stride of FB bytes
@@ -240,7 +257,8 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
 }
 
 template <int D, int VB, int KMODE, int NT>
-__global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) {
+__global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB, NT>::MIN_BLOCKS)
+    attn_split_kernel(AttnParams p) {
   using M = KeySpec<KMODE>;
   constexpr int KB = M::B;
   using SM = AttnSmem<D, KB, VB, NT>;
@@ -249,7 +267,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
   constexpr int DH = AttnSplit<D>::DH;
   constexpr int PDK_FULL = D * KB / 8, PDV_FULL = D * VB / 8, NG_FULL = D / kGroup;
   using VT = ValueTable<VB>;
-  constexpr int S = L::STAGES;
+  constexpr int S = SM::S;
+  constexpr int NW = SM::NW;
   const float kNegInf = -__int_as_float(0x7f800000);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_vtab = smem;
@@ -261,7 +280,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
   const int Rq = p.G * p.Nq;
   const int team = warp / SPL;           // warps sharing a tile
   const int half = warp % SPL;           // the head_dim slice of this warp
-  constexpr int kTeams = kAttnWarps / SPL;
+  constexpr int kTeams = NW / SPL;
 
   fill_value_table<VB>(s_vtab);
   pdl_launch_dependents();
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnParams p) 
 #pragma unroll
         for (int e = 0; e < 4; ++e) sfull[n][e] = __fadd_rn(sacc[n][0][e], sacc[n][1][e]);
       if constexpr (SPL > 1) {
-        float* slot = s_xchg + (k & 1) * (kAttnWarps * 32 * NT * 4);
+        float* slot = s_xchg + (k & 1) * (NW * 32 * NT * 4);
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -773,7 +792,7 @@ cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
   if (attr != cudaSuccess) return attr;
   static const int per_sm = [] {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<D, VB, KMODE, NT>, kAttnThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<D, VB, KMODE, NT>, L::Shape::THREADS,
                                                       L::SMEM) != cudaSuccess || n < 1)
       n = 1;
     return n;
@@ -784,13 +803,13 @@ cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
   // each team of warps gets at least kAttnMinTeamTiles tiles, so the per-block
   // start (value table, query operands) and the record merge stay small next
   // to its work when few heads hold many tiles
-  const long long teams = kAttnWarps / AttnSplit<D>::SPL;
+  const long long teams = L::NW / AttnSplit<D>::SPL;
   const long long by_work = (p.total_tiles + teams * kAttnMinTeamTiles - 1) / (teams * kAttnMinTeamTiles);
   if (grid > by_work) grid = by_work;
   if (grid > p.total_tiles) grid = p.total_tiles;
   if (grid < 1) grid = 1;
   p.grid = static_cast<int>(grid);
-  return launch_pdl_block(attn_split_kernel<D, VB, KMODE, NT>, p.grid, kAttnThreads, p, s, L::SMEM);
+  return launch_pdl_block(attn_split_kernel<D, VB, KMODE, NT>, p.grid, L::Shape::THREADS, p, s, L::SMEM);
 }
 
 template <int D, int VB, int NT>
