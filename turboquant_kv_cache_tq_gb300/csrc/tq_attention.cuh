@@ -55,18 +55,20 @@ constexpr int kAttnRows = kAttnMaxRows;  // query rows per kv head (M of the sco
 
 __host__ __device__ constexpr int attn_round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-template <int D, int KB, int VB>
+// Per-warp layout over D head_dim elements of a row whose scales and zero
+// points (SNG groups: the whole row's) are staged whole.
+template <int D, int KB, int VB, int SNG = D / kGroup>
 struct AttnLayout {
   static constexpr int NG = D / kGroup;
   static constexpr int PDK = D * KB / 8;
   static constexpr int PDV = D * VB / 8;
   // one stage: the tile's rows of the five packed buffers, back to back
-  static constexpr int KC = 0;                        // K codes  [16][PDK]
-  static constexpr int KS = KC + kAttnTile * PDK;     // K scales [16][NG] fp16
-  static constexpr int KZ = KS + kAttnTile * NG * 2;  // K zeros
-  static constexpr int VC = KZ + kAttnTile * NG * 2;  // V codes  [16][PDV]
-  static constexpr int VS = VC + kAttnTile * PDV;     // V scales
-  static constexpr int END = VS + kAttnTile * NG * 2;
+  static constexpr int KC = 0;                         // K codes  [16][PDK]
+  static constexpr int KS = KC + kAttnTile * PDK;      // K scales [16][SNG] fp16
+  static constexpr int KZ = KS + kAttnTile * SNG * 2;  // K zeros
+  static constexpr int VC = KZ + kAttnTile * SNG * 2;  // V codes  [16][PDV]
+  static constexpr int VS = VC + kAttnTile * PDV;      // V scales
+  static constexpr int END = VS + kAttnTile * SNG * 2;
   static constexpr int STAGE = attn_round_up(END + 16, 128);  // + room for word over-reads
   // value lookup table (see ValueTable): pairs of centroids for widths up to
   // 4 bits, once per half-warp lane; single centroids once per lane above
@@ -81,15 +83,18 @@ struct AttnLayout {
   static constexpr int KGROUPS = EK > kGroup ? EK / kGroup : 1;  // groups a lane's key range spans
 };
 
-// Head_dim split: at D = 512 a warp's registers cannot hold a whole row's
-// query operands and output accumulators, so two warps share each token tile,
-// one per half of head_dim: each decodes its half of the keys and values,
-// their partial scores are added through shared memory (both add the same two
-// terms, so both get the same scores and the same softmax), and each keeps
-// the output accumulators of its half. SPL warps per tile, DH elements each.
+// Head_dim split: above D = 128 a warp holding a whole row's query operands
+// and output accumulators needs 168 (D = 256) to 255 (D = 512) registers,
+// which leaves 8 to 12 warps per SM, so SPL = 2 warps share each token tile,
+// one per half of head_dim: each decodes its slice of the keys and values,
+// their partial scores are added through shared memory (all add the same
+// SPL terms in the same order, so all get the same scores and the same
+// softmax), and each keeps the output accumulators of its slice. (Four
+// 128-element slices at D = 512 measured slower: 37 -> 45 us on
+// [2, 2, 16384, 512], the four-way exchange every tile.)
 template <int D>
 struct AttnSplit {
-  static constexpr int SPL = D == 512 ? 2 : 1;
+  static constexpr int SPL = D > 128 ? 2 : 1;
   static constexpr int DH = D / SPL;
 };
 
@@ -106,15 +111,18 @@ struct AttnShape {
   static constexpr int NW = WIDE ? 8 : 4;
   static constexpr int THREADS = 32 * NW;
   static constexpr int S = (WIDE || DH >= 256) ? 2 : 3;
-  static constexpr int MIN_BLOCKS = WIDE ? 2 : 0;  // 0: no bound (the compiler's choice)
+  // 128 registers a thread for one query-row tile (NT = 1) over 128-element
+  // slices; wider slices or two tiles (NT = 2) need more and keep the
+  // compiler's choice (0: no bound)
+  static constexpr int MIN_BLOCKS = WIDE ? 2 : (NT == 1 && DH <= 128 ? 4 : 0);
 };
 
 // Block-level shared memory of the split kernel over the per-warp layout L:
-// value table | score exchange (SPL = 2) | ring of stages, later the merge
+// value table | score exchange (SPL > 1) | ring of stages, later the merge
 // area of one record per warp group.
 template <int D, int KB, int VB, int NT>
 struct AttnSmem {
-  using L = AttnLayout<AttnSplit<D>::DH, KB, VB>;
+  using L = AttnLayout<AttnSplit<D>::DH, KB, VB, D / kGroup>;
   using Shape = AttnShape<D, VB, NT>;
   static_assert(Shape::CENT == L::CENT, "one table size");
   static constexpr int NW = Shape::NW;
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
     const long long tok0 = static_cast<long long>(bh) * p.t_cap + t_beg;
     const int my_tiles = n_tiles > team ? (n_tiles - team + kTeams - 1) / kTeams : 0;
     // Step k of this warp handles tile team + kTeams k in stage k mod S (its
-    // half of each row when SPL = 2); every step commits one copy group
+    // slice of each row when SPL > 1); every step commits one copy group
     // (empty past the end).
     auto issue = [&](int k) {
       const long long tk = tok0 + static_cast<long long>(team + k * kTeams) * kAttnTile;
@@ -358,10 +366,10 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
           copy_region<kAttnTile * L::NG * 2>(dst + L::VS, p.v_scales + t * L::NG, lane);
         } else {
           copy_rows<kAttnTile, L::PDK, PDK_FULL>(dst + L::KC, p.k_codes + t * PDK_FULL + half * L::PDK, lane);
-          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::KS, p.k_scales + t * NG_FULL + half * L::NG, lane);
-          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::KZ, p.k_zeros + t * NG_FULL + half * L::NG, lane);
+          copy_region<kAttnTile * NG_FULL * 2>(dst + L::KS, p.k_scales + t * NG_FULL, lane);
+          copy_region<kAttnTile * NG_FULL * 2>(dst + L::KZ, p.k_zeros + t * NG_FULL, lane);
           copy_rows<kAttnTile, L::PDV, PDV_FULL>(dst + L::VC, p.v_codes + t * PDV_FULL + half * L::PDV, lane);
-          copy_rows<kAttnTile, L::NG * 2, NG_FULL * 2>(dst + L::VS, p.v_scales + t * NG_FULL + half * L::NG, lane);
+          copy_region<kAttnTile * NG_FULL * 2>(dst + L::VS, p.v_scales + t * NG_FULL, lane);
         }
       }
       cp_async_commit();
@@ -384,6 +392,7 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
       }
     const uint32_t vlane = VT::PAIRS ? 8u * (lane & 15) : 4u * lane;  // the lane's table replica
     constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
+    constexpr float kBias16 = 1024.0f + (M::SIGNED ? 128.0f : 0.0f);
 
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) issue(k);
@@ -400,6 +409,7 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
       // ---- keys: tokens g and g + 8, elements [c EK, (c+1) EK)
       uint32_t wk[2][L::NWK];
       float2 ks2[2][L::KGROUPS], kzb2[2][L::KGROUPS];
+      float kzh[2][L::KGROUPS];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int tau = g + 8 * hf;
@@ -413,8 +423,10 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
           const int grp = (c * L::EK) / kGroup + lg;
           const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + L::KS);
           const uint16_t* zr = reinterpret_cast<const uint16_t*>(st + L::KZ);
-          ks2[hf][lg] = f2(__half2float(__ushort_as_half(sc[tau * L::NG + grp])));
-          kzb2[hf][lg] = f2(__fsub_rn(__half2float(__ushort_as_half(zr[tau * L::NG + grp])), kBias));
+          ks2[hf][lg] = f2(__half2float(__ushort_as_half(sc[tau * NG_FULL + half * L::NG + grp])));
+          const float zp = __half2float(__ushort_as_half(zr[tau * NG_FULL + half * L::NG + grp]));
+          kzb2[hf][lg] = f2(__fsub_rn(zp, kBias));
+          kzh[hf][lg] = __fsub_rn(zp, kBias16);
         }
       }
       // scores S^T = K Q^T: M = the tile's 16 tokens, N = 8 query rows per tile
@@ -432,26 +444,30 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
         uint32_t af[2][2];  // [token g / g + 8][elements 0-1 / 2-3]
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          // four codes as the floats 1.5 * 2^23 + code (+ 128 for signed
-          // codes, whose bytes are offset by flipping their sign bits): one
-          // byte permute each for 8-bit codes
-          uint32_t u[4];
+          // RN(code + zero) for four codes (+ 128 for signed codes, whose
+          // bytes are offset by flipping their sign bits). 8-bit codes: one
+          // byte permute makes two fp16 values 1024 + byte, and one
+          // mixed-precision add each widens one and adds zero - 1024 -
+          // offset (exact: the zero point is an integer) in one rounding, on
+          // the FMA pipe; narrower codes: the floats 1.5 * 2^23 + code plus
+          // zero - 1.5 * 2^23 - offset. Then one rounding of the product
+          // with the scale (decodeKeys), then bf16.
+          float2 f01, f23;
           if constexpr (KB == 8) {
             const uint32_t w = wk[hf][j];
-            u[0] = __byte_perm(w, kMagicBits, 0x7640);
-            u[1] = __byte_perm(w, kMagicBits, 0x7641);
-            u[2] = __byte_perm(w, kMagicBits, 0x7642);
-            u[3] = __byte_perm(w, kMagicBits, 0x7643);
+            const uint32_t h01 = __byte_perm(w, 0x64646464u, 0x4140);
+            const uint32_t h23 = __byte_perm(w, 0x64646464u, 0x4342);
+            f01 = make_float2(add_f16_f32<false>(h01, kzh[hf][lg]), add_f16_f32<true>(h01, kzh[hf][lg]));
+            f23 = make_float2(add_f16_f32<false>(h23, kzh[hf][lg]), add_f16_f32<true>(h23, kzh[hf][lg]));
           } else {
+            uint32_t u[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) u[e] = kMagicBits | code_at<KB>(wk[hf], 4 * j + e);
+            f01 = add2(make_float2(__uint_as_float(u[0]), __uint_as_float(u[1])), kzb2[hf][lg]);
+            f23 = add2(make_float2(__uint_as_float(u[2]), __uint_as_float(u[3])), kzb2[hf][lg]);
           }
-          const float2 f01 = make_float2(__uint_as_float(u[0]), __uint_as_float(u[1]));
-          const float2 f23 = make_float2(__uint_as_float(u[2]), __uint_as_float(u[3]));
-          // + (zero - magic - offset) = code + zero exactly, then one
-          // rounding of the product with the scale (decodeKeys), then bf16
-          const float2 x01 = mul2(add2(f01, kzb2[hf][lg]), ks2[hf][lg]);
-          const float2 x23 = mul2(add2(f23, kzb2[hf][lg]), ks2[hf][lg]);
+          const float2 x01 = mul2(f01, ks2[hf][lg]);
+          const float2 x23 = mul2(f23, ks2[hf][lg]);
           af[hf][0] = pack_bf16x2(x01.x, x01.y);
           af[hf][1] = pack_bf16x2(x23.x, x23.y);
         }
@@ -460,9 +476,9 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
         for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
       }
 
-      // ---- the team's partial scores added (SPL = 2): each warp publishes
-      // its half's sums in slot k mod 2, and adds the other half's to its own
-      // (the same two terms in both warps, so the same sums)
+      // ---- the team's partial scores added (SPL > 1): each warp publishes
+      // its slice's sums in slot k mod 2 and adds all SPL slices in order
+      // (the same terms in the same order in every warp, so the same sums)
       float sfull[NT][4];
 #pragma unroll
       for (int n = 0; n < NT; ++n)
@@ -475,13 +491,18 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
 #pragma unroll
           for (int e = 0; e < 4; ++e) slot[((warp * NT + n) * 4 + e) * 32 + lane] = sfull[n][e];
         named_barrier(1 + team, 32 * SPL);
-        const int other = warp ^ 1;
+        // the slices' sums added in slice order (own slice from registers)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float o = slot[((other * NT + n) * 4 + e) * 32 + lane];
-            sfull[n][e] = half == 0 ? __fadd_rn(sfull[n][e], o) : __fadd_rn(o, sfull[n][e]);
+            float tot = 0.0f;
+#pragma unroll
+            for (int h = 0; h < SPL; ++h) {
+              const float o = h == half ? sfull[n][e] : slot[(((team * SPL + h) * NT + n) * 4 + e) * 32 + lane];
+              tot = h == 0 ? o : __fadd_rn(tot, o);
+            }
+            sfull[n][e] = tot;
           }
       }
 
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
         const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
         lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
         const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
-        float sc = __half2float(__ushort_as_half(sv[tau * L::NG + (g * L::EV) / kGroup]));
+        float sc = __half2float(__ushort_as_half(sv[tau * NG_FULL + half * L::NG + (g * L::EV) / kGroup]));
         if (!full) {
           // tokens past T or inside the left pad contribute exactly zero
           const int t = t0 + tau;

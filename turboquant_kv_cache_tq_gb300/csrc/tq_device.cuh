@@ -36,6 +36,20 @@ constexpr unsigned kFull = 0xffffffffu;
 // 1.5 * 2^23: for |t| < 2^22, RN(t + kMagic) = kMagic + rint(t) and the low
 // 22 bits of its encoding hold rint(t) (two's complement around 0x4B400000).
 constexpr float kMagic = 12582912.0f;
+
+// RN(h + c) for the fp16 value h held in the low (HI = false) or high half of
+// x: the mixed-precision add widens h exactly and rounds the sum once (an
+// FMA-pipe instruction at full rate).
+template <bool HI>
+__device__ __forceinline__ float add_f16_f32(uint32_t x, float c) {
+  float r;
+  if constexpr (HI) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}" : "=f"(r) : "r"(x), "f"(c));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}" : "=f"(r) : "r"(x), "f"(c));
+  }
+  return r;
+}
 constexpr uint32_t kMagicBits = 0x4B400000u;
 
 template <int D>

@@ -599,43 +599,54 @@ __device__ __forceinline__ void load_packed_item(const DecodeParams& p, bool is_
 }
 
 // K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
-// Codes become floats through the 1.5 * 2^23 encoding (exact for |q| < 2^22).
-// `prefetch` runs once the packed inputs are consumed (it may overwrite `in`).
-// K decode of one group: x = (code + zero) * scale, zero and scale from fp16.
-// Each code becomes the float 1.5 * 2^23 + bias + code (bias = 128 for
-// signed codes, whose bytes are first offset to [1, 255] by flipping their
-// sign bits), built directly as a bit pattern: a byte permute for 8-bit
-// codes, a shift and a mask otherwise. The zero point is an integer (or
-// +-Inf, or NaN), so zero - 1.5 * 2^23 - bias is exact and adding it to that
-// float gives RN(code + zero) in one rounding, as the page's sum does.
+// Signed codes are first offset to [0, 255] by flipping their bytes' sign
+// bits (code + 128). The zero point is an integer (or +-Inf, or NaN), so
+// zero minus an integer bias below 2^24 is exact, and RN(code + zero), the
+// page's sum, comes out of one rounding: for 8-bit codes a byte permute
+// makes two fp16 values 1024 + byte and a mixed-precision add widens each
+// and adds zero - 1024 - offset (FMA pipe); narrower codes become the floats
+// 1.5 * 2^23 + offset + code (a shift and a mask) plus zero - 1.5 * 2^23 -
+// offset. Then one rounding of the product with the scale.
 // `prefetch` runs once the packed inputs are consumed (it may overwrite `in`).
 template <int KMODE, int W, typename Prefetch>
 __device__ __forceinline__ void decode_key_item(const PackedIn<W>& in, float (&x)[32], Prefetch&& prefetch) {
   using M = KeySpec<KMODE>;
-  constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
+  constexpr float kOffset = M::SIGNED ? 128.0f : 0.0f;
   const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz & 0xffffu)));
   const float z = __half2float(__ushort_as_half(static_cast<uint16_t>(in.sz >> 16)));
-  const float zb = __fsub_rn(z, kBias);
-  uint32_t cb[32];
+  float cz[32];  // RN(code + zero)
   if constexpr (M::B == 8) {
+    const float zh = __fsub_rn(z, 1024.0f + kOffset);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t wk = M::SIGNED ? (in.w[k] ^ 0x80808080u) : in.w[k];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) cb[4 * k + j] = __byte_perm(wk, kMagicBits, 0x7640u | j);
+      const uint32_t h01 = __byte_perm(wk, 0x64646464u, 0x4140u);
+      const uint32_t h23 = __byte_perm(wk, 0x64646464u, 0x4342u);
+      cz[4 * k] = add_f16_f32<false>(h01, zh);
+      cz[4 * k + 1] = add_f16_f32<true>(h01, zh);
+      cz[4 * k + 2] = add_f16_f32<false>(h23, zh);
+      cz[4 * k + 3] = add_f16_f32<true>(h23, zh);
     }
+    prefetch();
   } else {
+    const float zb = __fsub_rn(z, kMagic + kOffset);
     uint32_t w[M::B];
 #pragma unroll
     for (int k = 0; k < M::B; ++k) w[k] = in.w[k];
+    uint32_t cb[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) cb[i] = unpack_code<M::B>(w, i) | kMagicBits;
+    prefetch();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = add2(make_float2(__uint_as_float(cb[2 * i]), __uint_as_float(cb[2 * i + 1])), f2(zb));
+      cz[2 * i] = f.x;
+      cz[2 * i + 1] = f.y;
+    }
   }
-  prefetch();
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float2 f = make_float2(__uint_as_float(cb[2 * i]), __uint_as_float(cb[2 * i + 1]));
-    const float2 g = mul2(add2(f, f2(zb)), f2(s));  // RN(RN(code + zero) * scale)
+    const float2 g = mul2(make_float2(cz[2 * i], cz[2 * i + 1]), f2(s));  // RN(RN(code + zero) * scale)
     x[2 * i] = g.x;
     x[2 * i + 1] = g.y;
   }
