@@ -178,14 +178,26 @@ def test_attention_argument_checks(L):
 
 def test_attention_workspace_size(L):
     assert L.tq_decode_attention_workspace_size(2, 2, 100, 1024) == -HEAD_DIM
-    assert L.tq_decode_attention_workspace_size(2, 2, 100, 512) % (16 * (512 + 2) * 4) == 0
     assert L.tq_decode_attention_workspace_size(-1, 2, 100, 128) == -INVALID
     assert L.tq_decode_attention_workspace_size(2, 0, 100, 128) == -INVALID
     rec = 16 * (128 + 2) * 4
-    n = L.tq_decode_attention_workspace_size(2, 2, 100, 128)
-    # one record per split block (at most 8 per SM) and per (batch, kv head)
-    assert n > 0 and n % rec == 0 and n >= (4 + 8) * rec
-    assert L.tq_decode_attention_workspace_size(2, 3, 100, 128) == n + 2 * rec
+    # many heads: one record per split block (at most 8 per SM) and per
+    # (batch, kv head), nothing else (a head has few records: one combine
+    # block per row tile)
+    big = L.tq_decode_attention_workspace_size(64, 64, 100, 128)
+    sms8 = big // rec - 64 * 64  # 8 x SMs
+    assert big % rec == 0 and sms8 > 0 and sms8 % 8 == 0
+    assert L.tq_decode_attention_workspace_size(64, 65, 100, 128) == big + 64 * rec
+    # few heads: the records, then the combine's partial sums (row tiles of
+    # 1024 / D rows for up to 16 query rows per kv head, 32 x 34 floats per
+    # chunk of 32 records, at most 8 chunks) and one ticket counter per tile
+    for B, H, D in [(2, 2, 128), (1, 1, 512), (4, 4, 256), (2, 2, 64), (3, 5, 128)]:
+        bhkv = B * H
+        recs = (sms8 + bhkv) * 16 * (D + 2) * 4
+        chunks = min(8, max(1, -(-(sms8 // bhkv + 2) // 32)))
+        tiles = -(-16 * bhkv * D // 1024)
+        extra = tiles * chunks * 32 * 34 * 4 + -(-tiles * 4 // 16) * 16 if chunks > 1 else 0
+        assert L.tq_decode_attention_workspace_size(B, H, 100, D) == recs + extra, (B, H, D)
 
 
 def test_cache_assemble_checks(L):

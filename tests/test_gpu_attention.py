@@ -94,8 +94,8 @@ def run_case(B, Hkv, G, Nq, T, D, kb, ks, vb, t_cap=None, left_pad=None, seed=0,
 @pytest.mark.parametrize("vb", [2, 3, 4, 5, 8])
 def test_matches_oracle_all_widths(D, vb):
     """Every key mode and value width; ragged token counts spanning several
-    16-token tiles and several split blocks. At head_dim 512 two warps share
-    each tile, one per half of head_dim."""
+    16-token tiles and several split blocks. At head_dim 256 and 512 two warps
+    share each tile, one per half of head_dim."""
     T = {64: 203, 128: 141, 256: 77, 512: 53}[D]
     for i, (kb, ks) in enumerate(KEY_MODES):
         got, want, vmax, _, _ = run_case(2, 2, 4, 1, T, D, kb, ks, vb, seed=10 * i + D + vb)
@@ -121,6 +121,22 @@ def test_head_dim_512_query_rows_and_pads(G, Nq, pads):
     ref = oracle.f32_to_bf16_bits(want.astype(np.float32))
     d = np.abs(oracle.bf16_bits_to_f32(_bits(got)).astype(np.float64) - oracle.bf16_bits_to_f32(ref))
     assert np.all(d <= 2.0 ** -7 * np.abs(want) + ATTN_TOL * np.repeat(vmax, G, axis=1)[:, :, None, None])
+
+
+@pytest.mark.parametrize("B,Hkv,G,Nq,T,D,vb,pads", [
+    (1, 1, 4, 1, 16384, 512, 2, None),
+    (2, 1, 8, 2, 20000, 128, 3, [0, 2500]),
+    (1, 2, 4, 1, 24000, 256, 4, None),
+    (1, 1, 4, 1, 60000, 64, 5, None),
+])
+def test_heads_over_many_split_blocks(B, Hkv, G, Nq, T, D, vb, pads):
+    """Few heads with long caches: each head's tiles spread over many split
+    blocks, so a row has many partial records and the combine merges them in
+    several chunks whose sums the last chunk to finish adds up (on a 152-SM
+    GB300: 3, 2, 2 and 4 chunks per row tile for these cases), with row tiles
+    spanning two heads, two query-row tiles and left pads."""
+    got, want, vmax, _, _ = run_case(B, Hkv, G, Nq, T, D, 8, True, vb, left_pad=pads, seed=T + D)
+    compare_attention(got.cpu().numpy(), want, vmax, G, "B%d Hkv%d G%d Nq%d T%d D%d" % (B, Hkv, G, Nq, T, D))
 
 
 @pytest.mark.parametrize("pads", [[0, 5, 17, 63], [16, 1, 40, 0], [89, 0, 3, 90]])

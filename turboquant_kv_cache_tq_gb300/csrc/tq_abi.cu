@@ -309,6 +309,28 @@ namespace {
 // touches, at most kAttnGridPerSm blocks per SM plus one per (batch, kv head).
 long long attn_records(long long bhkv) { return static_cast<long long>(kAttnGridPerSm) * sm_count() + bhkv; }
 
+// Workspace of the fused attention: the records, then (when a head can have
+// more records than one combine block takes) the combine's partial sums for
+// up to 16 * bhkv output rows (kAttnMaxRows query rows per kv head) in row
+// tiles of 1024 / D rows, then one ticket counter per row tile.
+struct AttnWorkspace {
+  long long records_bytes, partial_offset, counter_offset, bytes;
+  long long tiles;  // row tiles the partial area and the counters cover
+  int chunks;       // the most combine blocks per row tile any call of this size uses
+};
+AttnWorkspace attn_workspace(long long bhkv, long long D) {
+  AttnWorkspace w{};
+  w.records_bytes = attn_records(bhkv) * kAttnRecordFloats(D) * 4;
+  // a head's records: at most grid / bhkv + 2 (the split grid is at most
+  // kAttnGridPerSm blocks per SM)
+  w.chunks = attn_combine_chunks(static_cast<long long>(kAttnGridPerSm) * sm_count() / bhkv + 2);
+  w.tiles = (kAttnMaxRows * bhkv * D + 1023) / 1024;
+  w.partial_offset = w.records_bytes;
+  w.counter_offset = w.partial_offset + (w.chunks > 1 ? w.tiles * w.chunks * kCombinePartialFloats * 4 : 0);
+  w.bytes = w.counter_offset + (w.chunks > 1 ? (w.tiles * 4 + 15) / 16 * 16 : 0);
+  return w;
+}
+
 bool attn_head_dim_ok(int64_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
 }  // namespace
@@ -320,7 +342,7 @@ extern "C" int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, in
   if (!attn_head_dim_ok(D)) return -static_cast<int64_t>(TQ_ERR_HEAD_DIM);
   const long long bhkv = B * Hkv;
   if (bhkv > 0x7fffffffLL) return -static_cast<int64_t>(TQ_ERR_INVALID_ARG);
-  return static_cast<int64_t>(attn_records(bhkv) * kAttnRecordFloats(D) * 4);
+  return static_cast<int64_t>(attn_workspace(bhkv, D).bytes);
 }
 
 extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, int64_t Nq,
@@ -344,7 +366,8 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   if (t_cap > (1LL << 62) / (bhkv * 512)) return TQ_ERR_INVALID_ARG;
   const long long tiles_per_bh = (T + 15) / 16;
   if (bhkv * tiles_per_bh > (1LL << 40)) return TQ_ERR_INVALID_ARG;
-  const long long need = attn_records(bhkv) * kAttnRecordFloats(D) * 4;
+  const AttnWorkspace ws = attn_workspace(bhkv, D);
+  const long long need = ws.bytes;
   const void* ptrs[] = {q, k_codes, k_scales, k_zeros, v_codes, v_scales, out, workspace};
   for (const void* p : ptrs) {
     if (!p) return TQ_ERR_INVALID_ARG;
@@ -374,8 +397,12 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rot_scale = rotation_scale(D);
   p.cache_rows = bhkv * t_cap;
-  p.ws_records = workspace_bytes / (kAttnRecordFloats(D) * 4);
+  p.ws_records = ws.records_bytes / (kAttnRecordFloats(D) * 4);
   p.err = device_error_word();
+  p.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.partial_offset);
+  p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + ws.counter_offset);
+  p.chunks = 1;  // the launcher sets it from the split grid (at most ws.chunks)
+  p.combine_tiles = static_cast<int>((B * Hq * Nq * D + 1023) / 1024);
   const int kmode = key_mode(k_bits, k_signed);
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

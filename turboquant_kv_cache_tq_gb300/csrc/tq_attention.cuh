@@ -293,6 +293,9 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
   fill_value_table<VB>(s_vtab);
   pdl_launch_dependents();
   pdl_wait();
+  // the combine's tickets start at zero (it runs after this grid completes)
+  if (p.chunks > 1 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.combine_tiles; i += blockDim.x) p.counters[i] = 0u;
 
   // This block's share of the flattened (batch, kv head, tile) space, cut
   // into one segment per (batch, kv head) it touches; each segment ends in
@@ -682,15 +685,37 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
   }  // segments
 }
 
-// Merge of the chunk partials of one output row, normalisation, inverse
+// Merge of the split records of each output row, normalisation, inverse
 // rotation (unrotateValues: fp32 Hadamard butterflies, * 1/sqrt(D), signs)
-// and the store. A block takes one tile of output rows in the codec's lane
-// layout (lane l of a row owns elements [32 l, 32 l + 32)); its warps split
-// the row's chunk records between them (warp w merges records w, w + NW,
-// ...), since a head spread over many split blocks has many records: first
-// the largest running max over every record, then each warp's weighted sum,
-// then warp 0 adds the warps' sums in order and finishes the row.
-constexpr int kCombineWarps = 8;
+// and the store. Rows are taken in tiles of the codec's lane layout (lane l
+// of a row owns elements [32 l, 32 l + 32)), and each tile by p.chunks
+// blocks, block c merging the c-th of p.chunks equal runs of each row's
+// records (a head spread over many split blocks has many records). Partial
+// results (m, l, O: running max, weight sum and weighted row, relative to
+// exp2(m)) merge online: with M = max(m, m'), the sum is
+// exp2(m - M) (l, O) + exp2(m' - M) (l', O'), a factor taken as 0 for a
+// part whose m is -inf (it saw no valid key). Each warp merges records w,
+// w + NW, ... of the block's run in one pass, two records in flight; warp 0
+// merges the warps' results in warp order. With one chunk it finishes the
+// row. Otherwise it writes its (m, l, O) to the partial area and takes a
+// ticket (threadfence, then an atomic add on the tile's counter, which the
+// split pass zeroed): the block drawing the last ticket merges every
+// chunk's result in chunk order and finishes the row. No block waits on
+// another.
+struct OnlinePart {
+  float m, den, x[32];
+};
+
+__device__ __forceinline__ void online_merge(OnlinePart& a, float m, float den, const float (&x)[32]) {
+  const float kNegInf = -__int_as_float(0x7f800000);
+  const float mn = fmaxf(a.m, m);
+  const float fa = a.m == mn ? 1.0f : (a.m == kNegInf ? 0.0f : exp2f(__fsub_rn(a.m, mn)));
+  const float fb = m == kNegInf ? 0.0f : exp2f(__fsub_rn(m, mn));
+  a.den = __fadd_rn(__fmul_rn(a.den, fa), __fmul_rn(den, fb));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a.x[i] = __fadd_rn(__fmul_rn(a.x[i], fa), __fmul_rn(x[i], fb));
+  a.m = mn;
+}
 
 template <int D, bool F32>
 __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnParams p) {
@@ -699,8 +724,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnPa
   constexpr int NW = kCombineWarps;
   const float kNegInf = -__int_as_float(0x7f800000);
   __shared__ __align__(16) uint32_t s_sign[D / 2];
-  __shared__ float s_max[NW][32];
-  __shared__ float s_part[NW][32][33];  // per warp and lane: 32 weighted sums and the denominator
+  __shared__ float s_part[NW][34][32];  // per warp: 32 weighted sums, the weight sum and the max, per lane
+  __shared__ unsigned s_ticket;
   fill_sign_words<D>(s_sign);
   __syncthreads();
   pdl_launch_dependents();
@@ -709,8 +734,10 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnPa
   const int lane = threadIdx.x & 31;
   const int sub = lane / G::LPR;
   const int l = lane % G::LPR;
+  const int tile = blockIdx.x / p.chunks;
+  const int chunk = blockIdx.x - tile * p.chunks;
   const int rows = p.B * p.Hq * p.Nq;
-  const int row0 = blockIdx.x * G::RPW + sub;
+  const int row0 = tile * G::RPW + sub;
   const bool valid = row0 < rows;
   const int row = valid ? row0 : rows - 1;
   const int hq_n = p.Hq * p.Nq;
@@ -730,53 +757,77 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnPa
   }
   if (!TQ_CHECK(static_cast<long long>(c0) + bh + n_rec <= p.ws_records, p.err)) n_rec = 0;
   const float* recs = p.ws + (static_cast<long long>(c0) + bh) * REC;
-  float mx = kNegInf;
-  for (int s = warp; s < n_rec; s += NW) mx = fmaxf(mx, recs[s * REC + r]);
-  s_max[warp][lane] = mx;
-  __syncthreads();
+  // this block's run of the row's records, merged online by the warps
+  const int lo = static_cast<int>(static_cast<long long>(chunk) * n_rec / p.chunks);
+  const int hi = static_cast<int>(static_cast<long long>(chunk + 1) * n_rec / p.chunks);
+  OnlinePart acc;
+  acc.m = kNegInf;
+  acc.den = 0.0f;
 #pragma unroll
-  for (int w = 0; w < NW; ++w) mx = fmaxf(mx, s_max[w][lane]);
-  float x[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-  float den = 0.0f;
-  for (int s = warp; s < n_rec; s += NW) {
+  for (int i = 0; i < 32; ++i) acc.x[i] = 0.0f;
+#pragma unroll 2
+  for (int s = lo + warp; s < hi; s += NW) {
     const float* rec = recs + s * REC;
-    const float ms = rec[r];
-    if (ms == kNegInf) continue;
-    const float f = exp2f(__fsub_rn(ms, mx));
-    den = __fadd_rn(den, __fmul_rn(f, rec[16 + r]));
     const float4* o = reinterpret_cast<const float4*>(rec + 32 + r * D + kGroup * l);
+    float u[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 u = o[i];
-      x[4 * i] = __fadd_rn(x[4 * i], __fmul_rn(f, u.x));
-      x[4 * i + 1] = __fadd_rn(x[4 * i + 1], __fmul_rn(f, u.y));
-      x[4 * i + 2] = __fadd_rn(x[4 * i + 2], __fmul_rn(f, u.z));
-      x[4 * i + 3] = __fadd_rn(x[4 * i + 3], __fmul_rn(f, u.w));
+      const float4 v = o[i];
+      u[4 * i] = v.x; u[4 * i + 1] = v.y; u[4 * i + 2] = v.z; u[4 * i + 3] = v.w;
     }
+    online_merge(acc, rec[r], rec[16 + r], u);
   }
   if (warp != 0) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) s_part[warp][lane][i] = x[i];
-    s_part[warp][lane][32] = den;
+    for (int i = 0; i < 32; ++i) s_part[warp][i][lane] = acc.x[i];
+    s_part[warp][32][lane] = acc.den;
+    s_part[warp][33][lane] = acc.m;
   }
   __syncthreads();
   if (warp != 0) return;
-#pragma unroll
+#pragma unroll 1
   for (int w = 1; w < NW; ++w) {
+    float x[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __fadd_rn(x[i], s_part[w][lane][i]);
-    den = __fadd_rn(den, s_part[w][lane][32]);
+    for (int i = 0; i < 32; ++i) x[i] = s_part[w][i][lane];
+    online_merge(acc, s_part[w][33][lane], s_part[w][32][lane], x);
+  }
+  if (p.chunks > 1) {
+    // publish this chunk's (m, l, O) (float i of lane L at 32 i + L), take a ticket
+    float* mine = p.partials + (static_cast<long long>(tile) * p.chunks + chunk) * kCombinePartialFloats;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mine[32 * i + lane] = acc.x[i];
+    mine[32 * 32 + lane] = acc.den;
+    mine[32 * 33 + lane] = acc.m;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) s_ticket = atomicAdd(p.counters + tile, 1u);
+    __syncwarp();
+    if (s_ticket != static_cast<unsigned>(p.chunks - 1)) return;  // not the last chunk to finish
+    __threadfence();
+    const float* all = p.partials + static_cast<long long>(tile) * p.chunks * kCombinePartialFloats;
+    acc.m = kNegInf;
+    acc.den = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc.x[i] = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < p.chunks; ++c) {
+      const float* part = all + static_cast<long long>(c) * kCombinePartialFloats;
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __ldcg(part + 32 * i + lane);
+      online_merge(acc, __ldcg(part + 32 * 33 + lane), __ldcg(part + 32 * 32 + lane), x);
+    }
   }
   uint32_t Sg[16];
   load_sign_words(s_sign, l, Sg);
   // a row with no valid key is zero
+  const float den = acc.den;
   const bool empty = den == 0.0f;
   float2 Y[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q)
-    Y[q] = empty ? make_float2(0.0f, 0.0f) : make_float2(__fdiv_rn(x[q], den), __fdiv_rn(x[q + 16], den));
+    Y[q] = empty ? make_float2(0.0f, 0.0f) : make_float2(__fdiv_rn(acc.x[q], den), __fdiv_rn(acc.x[q + 16], den));
   hadamard_row<G::LPR>(Y, l);
 #pragma unroll
   for (int q = 0; q < 16; ++q) Y[q] = mul2(Y[q], f2(p.rot_scale));
@@ -830,6 +881,8 @@ cudaError_t launch_attn_split_t(AttnParams& p, cudaStream_t s) {
   if (grid > p.total_tiles) grid = p.total_tiles;
   if (grid < 1) grid = 1;
   p.grid = static_cast<int>(grid);
+  // a head's records: at most grid / (B Hkv) + 2
+  p.chunks = attn_combine_chunks(grid / (static_cast<long long>(p.B) * p.Hkv) + 2);
   return launch_pdl_block(attn_split_kernel<D, VB, KMODE, NT>, p.grid, L::Shape::THREADS, p, s, L::SMEM);
 }
 
@@ -864,11 +917,12 @@ cudaError_t launch_attention(const AttnParams& params, int v_bits, int kmode, bo
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Nq;
-  const int tiles = static_cast<int>((rows + Geo<D>::RPW - 1) / Geo<D>::RPW);  // one block per row tile
+  const long long tiles = (rows + Geo<D>::RPW - 1) / Geo<D>::RPW;  // p.chunks blocks per row tile
+  const int grid = static_cast<int>(tiles * p.chunks);
   if (out_bf16) {
-    e = launch_pdl(attn_combine_kernel<D, false>, tiles, p, s, 0, 32 * kCombineWarps);
+    e = launch_pdl(attn_combine_kernel<D, false>, grid, p, s, 0, 32 * kCombineWarps);
   } else {
-    e = launch_pdl(attn_combine_kernel<D, true>, tiles, p, s, 0, 32 * kCombineWarps);
+    e = launch_pdl(attn_combine_kernel<D, true>, grid, p, s, 0, 32 * kCombineWarps);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -87,6 +87,20 @@ constexpr long long kAttnRecordFloats(long long D) { return kAttnMaxRows * (D + 
 // Split blocks per SM at most; the workspace holds (this * SMs + B * Hkv)
 // records.
 constexpr int kAttnGridPerSm = 8;
+// Combine: warps per block; a head's records are merged by up to
+// kCombineMaxChunks blocks of kCombineChunkRecords records each (four per
+// warp), whose partial results (32 lanes x 34 floats per row tile and
+// block: 32 weighted sums, the weight sum, the running max) the last of them
+// to finish merges.
+constexpr int kCombineWarps = 8;
+constexpr int kCombineMaxChunks = 8;
+constexpr int kCombineChunkRecords = 4 * kCombineWarps;
+constexpr int kCombinePartialFloats = 32 * 34;
+// Chunks for heads of at most n records.
+inline int attn_combine_chunks(long long n) {
+  const long long c = (n + kCombineChunkRecords - 1) / kCombineChunkRecords;
+  return static_cast<int>(c < 1 ? 1 : (c > kCombineMaxChunks ? kCombineMaxChunks : c));
+}
 
 struct AttnParams {
   const uint16_t* q;    // [B, Hq, Nq, D] bf16 queries
@@ -108,6 +122,10 @@ struct AttnParams {
   long long cache_rows; // B * Hkv * t_cap (debug checks)
   long long ws_records; // records the workspace holds (debug checks)
   unsigned* err;        // the library's device error word, or null
+  float* partials;      // combine partial sums [combine_tiles][chunks][32 x 33] (chunks > 1)
+  unsigned* counters;   // combine tickets per row tile, zeroed by the split pass (chunks > 1)
+  int chunks;           // combine blocks per row tile (set by the launcher)
+  int combine_tiles;    // row tiles of the output (B * Hq * Nq rows)
 };
 
 // Launchers per head_dim, one translation unit per input or output type (and
