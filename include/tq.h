@@ -156,10 +156,12 @@ TQ_API tq_status tq_lloyd_max_index(const float* u, int64_t n, int v_bits, uint8
  *   workspace, workspace_bytes: caller-owned device scratch of at least
  *            tq_decode_attention_workspace_size(B, Hkv, T, D) bytes (16-byte
  *            aligned) for the partial results of the split pass (one record
- *            per split block and kv head it covers); it must not be in use by
- *            another call still running, and needs no initialisation.
- * Limits: D in {64, 128, 256, 512} (else TQ_ERR_HEAD_DIM; at 512 two warps
- * share each token tile, one per half of head_dim); Hq a multiple of Hkv
+ *            per split block and kv head it covers) and, when a head can
+ *            have more than 32 records, the combine's per-chunk results and
+ *            ticket counters (zeroed by the split pass); it must not be in
+ *            use by another call still running, and needs no initialisation.
+ * Limits: D in {64, 128, 256, 512} (else TQ_ERR_HEAD_DIM; at 256 and 512 two
+ * warps share each token tile, one per half of head_dim); Hq a multiple of Hkv
  * and (Hq / Hkv) * Nq <= 16 (else TQ_ERR_INVALID_ARG); t_cap % 16 == 0
  * (else TQ_ERR_ALIGNMENT). B == 0 is a no-op. Two kernels are enqueued on
  * `stream`: the split pass, which cuts the (batch, kv head, 16-token tile)
@@ -194,7 +196,9 @@ TQ_API int64_t tq_decode_attention_workspace_size(int64_t B, int64_t Hkv, int64_
  *     that of tq_decode_attention (an empty batch, B == 0, returns TQ_OK
  *     without looking at the scratch). The need is one partial record of
  *     16 * (D + 2) floats per split block and per (batch, kv head) pair, with
- *     at most 8 split blocks per SM, so the largest B * Hkv served is
+ *     at most 8 split blocks per SM (plus, for fewer than 8 * SMs / 30
+ *     pairs, at most 8 * 34 * 32 floats per 1024 / D output rows for the
+ *     combine), so the largest B * Hkv served is
  *     floor(TQ_ATTENTION_NOALLOC_SCRATCH_BYTES / (64 * (D + 2))) - 8 * SMs:
  *     on a 152-SM GB300 that is 14671, 6849, 2848 and 824 pairs at head_dim
  *     64, 128, 256 and 512, independent of the number of tokens.
