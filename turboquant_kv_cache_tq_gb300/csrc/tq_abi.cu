@@ -403,6 +403,7 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + ws.counter_offset);
   p.chunks = 1;  // the launcher sets it from the split grid (at most ws.chunks)
   p.combine_tiles = static_cast<int>((B * Hq * Nq * D + 1023) / 1024);
+  p.vtab_stride = 128;
   const int kmode = key_mode(k_bits, k_signed);
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

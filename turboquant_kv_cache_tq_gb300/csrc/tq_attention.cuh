@@ -189,7 +189,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -248,6 +248,16 @@ __device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int bit,
   return (x & kMask) | lane_off;
 }
 
+// The same address for a byte-aligned 8-bit field (byte k, compile-time): a
+// byte permute and a multiply-add by the table's entry stride, a runtime
+// value so the multiply stays on the FMA pipe (a shift and a mask would both
+// take the ALU pipe, the busiest of this kernel).
+template <int NW>
+__device__ __forceinline__ uint32_t byte_field_addr(const uint32_t (&w)[NW], int k, uint32_t stride,
+                                                    uint32_t lane_off) {
+  return __byte_perm(w[k >> 2], 0u, 0x4440u | static_cast<uint32_t>(k & 3)) * stride + lane_off;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   // ex2.approx: relative error below 2^-22; results below 2^-126 flush to
   // zero, which only drops weights under 2^-126 of the row's largest one
@@ -260,7 +270,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // lane / 4, columns 2 (lane % 4) and 2 (lane % 4) + 1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
 
@@ -394,6 +404,7 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
         l_run[n][x] = 0.0f;
       }
     const uint32_t vlane = VT::PAIRS ? 8u * (lane & 15) : 4u * lane;  // the lane's table replica
+    const uint32_t vstride = p.vtab_stride;
     constexpr float kBias = kMagic + (M::SIGNED ? 128.0f : 0.0f);
     constexpr float kBias16 = 1024.0f + (M::SIGNED ? 128.0f : 0.0f);
 
@@ -479,6 +490,24 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
         for (int n = 0; n < NT; ++n) mma_bf16_16816(sacc[n][j & 1], a, qf[j][n][0], qf[j][n][1]);
       }
 
+      // ---- values: tokens 2c, 2c + 1, 2c + 8, 2c + 9, elements [g EV, (g+1) EV):
+      // packed words and scales loaded here, ahead of the softmax, whose
+      // shuffles and exponentials their shared-memory latency then overlaps
+      uint32_t wv[4][L::NWV];
+      float2 vs2[4];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
+        lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
+        const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
+        float sc = __half2float(__ushort_as_half(sv[tau * NG_FULL + half * L::NG + (g * L::EV) / kGroup]));
+        if (!full) {
+          // tokens past T or inside the left pad contribute exactly zero
+          const int t = t0 + tau;
+          sc = (t >= t_lo && t < p.T) ? sc : 0.0f;
+        }
+        vs2[k4] = f2(sc);
+      }
       // ---- the team's partial scores added (SPL > 1): each warp publishes
       // its slice's sums in slot k mod 2 and adds all SPL slices in order
       // (the same terms in the same order in every warp, so the same sums)
@@ -575,22 +604,6 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
           blo[n][hf] = movmatrix_trans(lo);
         }
 
-      // ---- values: tokens 2c, 2c + 1, 2c + 8, 2c + 9, elements [g EV, (g+1) EV)
-      uint32_t wv[4][L::NWV];
-      float2 vs2[4];
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const int tau = 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-        lds_words<L::NWV, L::VALIGN>(st + L::VC + tau * L::PDV, g * (L::EV * VB / 8), wv[k4]);
-        const uint16_t* sv = reinterpret_cast<const uint16_t*>(st + L::VS);
-        float sc = __half2float(__ushort_as_half(sv[tau * NG_FULL + half * L::NG + (g * L::EV) / kGroup]));
-        if (!full) {
-          // tokens past T or inside the left pad contribute exactly zero
-          const int t = t0 + tau;
-          sc = (t >= t_lo && t < p.T) ? sc : 0.0f;
-        }
-        vs2[k4] = f2(sc);
-      }
 #pragma unroll
       for (int i = 0; i < DH / 16; ++i) {
         // elements 2i, 2i + 1 of each token: RN(centroid * scale), to bf16
@@ -598,7 +611,12 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           float2 cc;
-          if constexpr (VT::PAIRS) {
+          if constexpr (VB == 4) {
+            cc = *reinterpret_cast<const float2*>(s_vtab + byte_field_addr(wv[k4], i, vstride, vlane));
+          } else if constexpr (VB == 8) {
+            cc = make_float2(*reinterpret_cast<const float*>(s_vtab + byte_field_addr(wv[k4], 2 * i, vstride, vlane)),
+                             *reinterpret_cast<const float*>(s_vtab + byte_field_addr(wv[k4], 2 * i + 1, vstride, vlane)));
+          } else if constexpr (VT::PAIRS) {
             cc = *reinterpret_cast<const float2*>(s_vtab + field_addr<2 * VB, 7>(wv[k4], 2 * i * VB, vlane));
           } else {
             cc = make_float2(*reinterpret_cast<const float*>(s_vtab + field_addr<VB, 7>(wv[k4], 2 * i * VB, vlane)),
