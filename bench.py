@@ -663,7 +663,9 @@ def copy_floor(dev, reps: int):
     """Per-launch time of torch's device copy moving the bytes of one
     Llama-3-8B-shaped layer encode (11.67 MB read + 11.67 MB written), 32
     distinct buffers in one CUDA graph, the way the bench times the codec:
-    what a plain memory-bound kernel reaches at this launch size."""
+    what a plain memory-bound kernel reaches at this launch size; then the
+    per-launch time of 32 one-element kernels, and of 32 codec launches on 8
+    tokens of the layer shape (the codec's fixed cost per launch)."""
     n = 23330816 // 4  # int16 elements per copy
     srcs = [torch.zeros(n, dtype=torch.int16, device=dev) for _ in range(32)]
     dsts = [torch.empty_like(x) for x in srcs]
@@ -712,6 +714,39 @@ def copy_floor(dev, reps: int):
     e1.synchronize()
     print("launch floor (32 one-element kernels in a CUDA graph): %.2f us per launch"
           % (1e3 * e0.elapsed_time(e1) / reps / 32))
+    # the codec's own fixed cost: 32 encode / decode launches of 8 tokens of
+    # the layer shape (64 rows) in a CUDA graph
+    import turboquant_kv_cache_tq_gb300 as tq
+
+    layers = []
+    for _ in range(32):
+        k = torch.randn((1, 8, 8, 128), device=dev).to(torch.bfloat16)
+        v = torch.randn((1, 8, 8, 128), device=dev).to(torch.bfloat16)
+        layers.append((k, v, tq.alloc_cache(1, 8, 8, 128, 8, 3, device=dev), torch.empty_like(k), torch.empty_like(v)))
+
+    def per_launch(fn):
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.synchronize(dev)
+        g3 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g3, stream=s):
+            fn()
+        for _ in range(5):
+            g3.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(reps):
+                g3.replay()
+        e1.record(s)
+        e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps / 32
+
+    enc = per_launch(lambda: [tq.tq_encode_kv(k, v, 8, True, 3, c, stream=s) for k, v, c, _, _ in layers])
+    dec = per_launch(lambda: [tq.tq_decode_kv(c, 8, 8, True, 3, k_out=ko, v_out=vo, stream=s)
+                              for _, _, c, ko, vo in layers])
+    print("codec fixed cost (32 launches of 8 tokens x 8 kv heads in a CUDA graph): encode %.2f us, decode %.2f us "
+          "per launch" % (enc, dec))
 
 
 def host_link_floor(dev, reps: int):
@@ -773,13 +808,15 @@ def run_case(name: str, reps: int, v_bits=None, batch=None):
         return
     e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
     if name == "attention":
-        B, H, T, D, G, vb = 32, 8, 8256, 128, 4, 3
+        B, H, T, D, G = 32 if batch is None else batch, 8, 8256, 128, 4
+        vb = 3 if v_bits is None else v_bits
         cache = tq.alloc_cache(B, H, T, D, 8, vb, device=dev)
         g = torch.Generator(device=dev).manual_seed(0)
         for b0 in range(0, B, 4):  # encode in slices to keep the footprint small
-            k = (0.5 * torch.randn((4, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
-            v = (0.5 * torch.randn((4, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
-            tq.tq_encode_kv(k, v, 8, True, vb, {n: t[b0:b0 + 4] for n, t in cache.items()})
+            nb = min(4, B - b0)
+            k = (0.5 * torch.randn((nb, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
+            v = (0.5 * torch.randn((nb, H, T, D), generator=g, device=dev)).to(torch.bfloat16)
+            tq.tq_encode_kv(k, v, 8, True, vb, {n: t[b0:b0 + nb] for n, t in cache.items()})
             del k, v
         q = torch.randn((B, H * G, 1, D), generator=g, device=dev).to(torch.bfloat16)
         out = torch.empty_like(q)
@@ -790,7 +827,7 @@ def run_case(name: str, reps: int, v_bits=None, batch=None):
             tq.tq_decode_attention(q, cache, T, 8, True, vb, out=out, workspace=work)
             e[r][1].record()
         torch.cuda.synchronize()
-        print("attention [32,8,8256,128] k8s v3: %.1f us" % _median_us(e))
+        print("attention [%d,8,8256,128] k8s v%d: %.1f us" % (B, vb, _median_us(e)))
         return
     w = WORKLOADS[name]
     B = w.B if batch is None else batch
