@@ -404,6 +404,7 @@ extern "C" tq_status tq_decode_attention(const void* q, int64_t B, int64_t Hq, i
   p.chunks = 1;  // the launcher sets it from the split grid (at most ws.chunks)
   p.combine_tiles = static_cast<int>((B * Hq * Nq * D + 1023) / 1024);
   p.vtab_stride = 128;
+  p.partial_floats = (ws.counter_offset - ws.partial_offset) / 4;
   const int kmode = key_mode(k_bits, k_signed);
   const bool bf16 = out_dtype == TQ_BF16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(AttnShape<D, VB, NT>::THREADS, AttnShape<D, VB
   pdl_launch_dependents();
   pdl_wait();
   // the combine's tickets start at zero (it runs after this grid completes)
-  if (p.chunks > 1 && blockIdx.x == 0)
+  if (p.chunks > 1 && blockIdx.x == 0 &&
+      TQ_CHECK(static_cast<long long>(p.combine_tiles) * p.chunks * kCombinePartialFloats <= p.partial_floats, p.err))
     for (int i = threadIdx.x; i < p.combine_tiles; i += blockDim.x) p.counters[i] = 0u;
 
   // This block's share of the flattened (batch, kv head, tile) space, cut
@@ -811,6 +812,10 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(AttnPa
     online_merge(acc, s_part[w][33][lane], s_part[w][32][lane], x);
   }
   if (p.chunks > 1) {
+    if (!TQ_CHECK(tile < p.combine_tiles &&
+                      (static_cast<long long>(tile) + 1) * p.chunks * kCombinePartialFloats <= p.partial_floats,
+                  p.err))
+      return;
     // publish this chunk's (m, l, O) (float i of lane L at 32 i + L), take a ticket
     float* mine = p.partials + (static_cast<long long>(tile) * p.chunks + chunk) * kCombinePartialFloats;
 #pragma unroll

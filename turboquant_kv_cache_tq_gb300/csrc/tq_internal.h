@@ -126,6 +126,7 @@ struct AttnParams {
   unsigned* counters;   // combine tickets per row tile, zeroed by the split pass (chunks > 1)
   int chunks;           // combine blocks per row tile (set by the launcher)
   int combine_tiles;    // row tiles of the output (B * Hq * Nq rows)
+  long long partial_floats;  // floats the partial area holds (debug checks)
   unsigned vtab_stride; // 128: bytes between entries of the value lookup table
 };
 
