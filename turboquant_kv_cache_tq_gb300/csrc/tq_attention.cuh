@@ -46,6 +46,11 @@
 
 namespace tq {
 
+#ifndef TQ_ATTN_STAGES
+// ring stages of a four-warp block at <= 128 elements per warp (two measured
+// faster than three: long-context v3 attention 119.4 -> 117.7 us)
+#define TQ_ATTN_STAGES 2
+#endif
 #ifndef TQ_ATTN_MIN_TEAM_TILES
 #define TQ_ATTN_MIN_TEAM_TILES 8
 #endif
@@ -110,7 +115,7 @@ struct AttnShape {
   static constexpr bool WIDE = DH <= 128 && CENT >= 32768 && NT == 1;
   static constexpr int NW = WIDE ? 8 : 4;
   static constexpr int THREADS = 32 * NW;
-  static constexpr int S = (WIDE || DH >= 256) ? 2 : 3;
+  static constexpr int S = (WIDE || DH >= 256) ? 2 : TQ_ATTN_STAGES;
   // 128 registers a thread for one query-row tile (NT = 1) over 128-element
   // slices; wider slices or two tiles (NT = 2) need more and keep the
   // compiler's choice (0: no bound)

@@ -33,6 +33,21 @@
 // Included by tq_kernels.cuh after the per-lane decode and the launch helpers.
 #pragma once
 
+// Ring sizes and the 8-bit-value occupancy bound. Measured alternatives on
+// the long-context v8 / v3 decode (278 / 254 us as set): 2 input stages
+// 279 / 255, 8 input stages 395 / 275 (fewer blocks fit), 1 output buffer
+// 280 / 255, 4 output buffers 403 / 279, 3 blocks per SM at 8-bit values
+// (80 registers; shared memory still fits only 2) 293 / 254.
+#ifndef TQ_DECODE_BULK_STAGES_IN
+#define TQ_DECODE_BULK_STAGES_IN 4
+#endif
+#ifndef TQ_DECODE_BULK_STAGES_OUT
+#define TQ_DECODE_BULK_STAGES_OUT 2
+#endif
+#ifndef TQ_DECODE_BULK_V8_MIN_BLOCKS
+#define TQ_DECODE_BULK_V8_MIN_BLOCKS 2
+#endif
+
 namespace tq {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -152,8 +167,8 @@ template <int D, int VB, int KMODE>
 struct BulkDecodeShape {
   static constexpr int kKB = KeySpec<KMODE>::B;
   static constexpr int kW = kKB > VB ? kKB : VB;
-  static constexpr int kStagesIn = 4;   // a power of two
-  static constexpr int kStagesOut = 2;  // bulk groups a warp keeps in flight
+  static constexpr int kStagesIn = TQ_DECODE_BULK_STAGES_IN;    // a power of two
+  static constexpr int kStagesOut = TQ_DECODE_BULK_STAGES_OUT;  // bulk groups a warp keeps in flight
   static constexpr int kCodeBytes = 128 * kW;  // 32 groups x 4 W bytes
   static constexpr int kScaleOff = kCodeBytes;
   static constexpr int kZeroOff = kCodeBytes + 64;
@@ -163,7 +178,7 @@ struct BulkDecodeShape {
   static constexpr int kWarps = kThreads / 32;
   static constexpr int kBarOff = kWarps * kWarpBytes;
   static constexpr int kSmem = kBarOff + kWarps * kStagesIn * 8;
-  static constexpr int kMinBlocks = VB == 8 ? 2 : 3;
+  static constexpr int kMinBlocks = VB == 8 ? TQ_DECODE_BULK_V8_MIN_BLOCKS : 3;
 };
 
 // Polls of a stage's mbarrier before a warp gives up (each poll may suspend
