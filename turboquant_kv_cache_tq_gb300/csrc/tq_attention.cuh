@@ -15,31 +15,37 @@
 //   V_rot[t] = bf16(RN(centroid[idx] * scale_v))      (decodeValuesRotated)
 // over the valid keys t of query row q: left_pad[b] <= t <= T - Nq + n.
 //
-// Split kernel: one block of four warps per (batch, kv head, chunk of
-// tokens). A warp streams 16-token tiles of the five packed buffers through
-// its own ring of shared-memory stages (cp.async, 16-byte pieces) and, per
-// tile:
-//   scores  S = Q K^T on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-//           accumulate): M = 16 query rows (the Hq/Hkv heads of the group
-//           times Nq tokens), N = 8 tokens, K = 16 head_dim elements. The
-//           head_dim order inside the contraction is permuted so that the
-//           four lanes sharing a token each own a quarter of the row
-//           (D/4 consecutive elements: exactly one quantisation group at
-//           D = 128), so a lane decodes its own contiguous codes with its own
-//           group scale and zero point, and the bf16 products are exact;
-//   softmax online in fp32 (exp2 of scores pre-scaled by log2 e), per row;
+// Split kernel: the flattened (batch, kv head, 16-token tile) space is cut
+// evenly over one wave of blocks of four warps (eight where the value table
+// is 32 KB); a block's share is cut into per-head segments. A warp streams
+// 16-token tiles of the five packed buffers through its own two-stage ring of
+// shared memory (cp.async, 16-byte pieces) and, per tile:
+//   scores  S^T = K Q^T on the tensor cores (mma.sync m16n8k16, bf16 in,
+//           fp32 accumulate): M = the tile's 16 tokens, N = 8 query rows
+//           (the Hq/Hkv heads of the group times Nq tokens) per row tile,
+//           K = 16 head_dim elements. The head_dim order inside the
+//           contraction is permuted so that the four lanes sharing a token
+//           each own a quarter of the row (D/4 consecutive elements: one
+//           quantisation group at D = 128), so a lane decodes its own
+//           contiguous codes with its own group scale and zero point, and the
+//           bf16 products are exact; the queries stay in registers;
+//   softmax online in fp32 (exp2 of scores pre-scaled by log2 e), per query
+//           row;
 //   values  O^T += V^T P^T, M = 16 head_dim elements, N = 8 query rows,
-//           K = 16 tokens. P comes straight from the score accumulators (the
-//           accumulator layout of one MMA is the operand layout of the
-//           other), split as P = P_hi + P_lo in bf16 (two MMAs), which keeps
-//           the weights exact to about 2^-18; the values are exact in bf16.
-// The four warps' partial (max, sum, O) are merged in shared memory and the
-// block writes one partial record to the workspace.
+//           K = 16 tokens. P comes straight from the score accumulators
+//           (transposed 8x8 by movmatrix), split as P = P_hi + P_lo in bf16
+//           (two MMAs), which keeps the weights exact to about 2^-18; the
+//           values are exact in bf16.
+// Above D = 128 two warps share each tile, one per half of head_dim (see
+// AttnSplit). At the end of a segment the warps' partial (max, sum, O) are
+// merged in shared memory and the block writes one partial record to the
+// workspace.
 //
-// Combine kernel: per output row, merges the chunk partials, divides by the
-// softmax denominator and applies the inverse rotation in fp32 (the Hadamard
-// butterflies of the codec, * 1/sqrt(D), then the signs: unrotateValues),
-// storing fp32 or bf16.
+// Combine kernel: merges each output row's records (in chunks over several
+// blocks when a head has many, the last block to finish adding the chunks'
+// results), divides by the softmax denominator and applies the inverse
+// rotation in fp32 (the Hadamard butterflies of the codec, * 1/sqrt(D), then
+// the signs: unrotateValues), storing fp32 or bf16.
 #pragma once
 
 #include "tq_kernels.cuh"
