@@ -58,7 +58,10 @@ namespace tq {
 #define TQ_ATTN_STAGES 2
 #endif
 #ifndef TQ_ATTN_MIN_TEAM_TILES
-#define TQ_ATTN_MIN_TEAM_TILES 8
+// fewest tiles per team of warps when heads are few and long (4: [4, 4, 8192,
+// 256] v4 30.5 -> 28.1 us against 8 since the chunked combine; 2 the same as
+// 4; 12 slower, 39.6 us)
+#define TQ_ATTN_MIN_TEAM_TILES 4
 #endif
 constexpr long long kAttnMinTeamTiles = TQ_ATTN_MIN_TEAM_TILES;
 constexpr int kAttnTile = 16;  // tokens per warp step
