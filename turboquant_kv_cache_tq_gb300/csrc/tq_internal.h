@@ -94,7 +94,12 @@ constexpr int kAttnGridPerSm = 8;
 // to finish merges.
 constexpr int kCombineWarps = 8;
 constexpr int kCombineMaxChunks = 8;
-constexpr int kCombineChunkRecords = 4 * kCombineWarps;
+#ifndef TQ_COMBINE_CHUNK_RECORDS
+// (8, 16, 64 measured: within a microsecond either way on the head_dim 256 and
+// 512 attention steps, none better on both)
+#define TQ_COMBINE_CHUNK_RECORDS 32
+#endif
+constexpr int kCombineChunkRecords = TQ_COMBINE_CHUNK_RECORDS;
 constexpr int kCombinePartialFloats = 32 * 34;
 // Chunks for heads of at most n records.
 inline int attn_combine_chunks(long long n) {
