@@ -17,8 +17,11 @@
 // group sits at byte 4 * bits * L of the tile's packed codes, at 2 L of its
 // scales and zero points, and at 64 L (bf16) of its decoded output, whatever
 // D. Each warp owns kStagesIn input stages (codes | scales | zero points) and
-// kStagesOut output buffers; items are taken in the per-lane kernel's
-// interleaved order (item gw + k n, a V item when (item ^ k) is odd).
+// kStagesOut output buffers; items are taken in the encode's orders
+// (ItemOrder): interleaved (item gw + k n, a V item when (item ^ k) is odd)
+// for long launches, all V items first in snake order for launches of at
+// most kSnakeSteps steps per warp, whose end is set by the warps with one
+// step more than the rest.
 //
 // Used when every tile's rows are contiguous and 16-byte aligned in all five
 // packed buffers, the outputs are bf16 and every buffer is device memory
@@ -185,7 +188,7 @@ struct BulkDecodeShape {
 // the warp for a short hardware time slice; about a second in all).
 constexpr unsigned kBulkWaitLimit = 1u << 20;
 
-template <int D, int VB, int KMODE, bool ROT>
+template <int D, int VB, int KMODE, bool ROT, bool SNAKE>
 __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMinBlocks))
     decode_bulk_kernel(DecodeParams p) {
   using G = Geo<D>;
@@ -214,13 +217,17 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
 
   const int l = lane % G::LPR;
   const int n_warps = gridDim.x * (blockDim.x >> 5);
-  const int items = 2 * (p.rows / G::RPW);  // every tile is full (checked on the host)
+  const int tiles = p.rows / G::RPW;  // every tile is full (checked on the host)
+  const int items = 2 * tiles;
   const int gw = warp_index();
+  // the encode's item orders: interleaved K and V items for long launches,
+  // all V items first in snake order for short ones (see ItemOrder)
+  const ItemOrder<SNAKE> ord{n_warps, gw, tiles};
   // Lane 0 issues the copies of step k into stage k mod S.
   auto issue = [&](int k) {
-    const int it = gw + k * n_warps;
+    const int it = ord.item(k);
     if (lane != 0 || it >= items) return;
-    const int r0 = (it >> 1) * G::RPW;
+    const int r0 = ord.tile(it) * G::RPW;
     const int bh = fast_div(r0, p.tdiv);
     const long long irow = static_cast<long long>(bh) * p.t_cap + (r0 - bh * p.T);
     const uint32_t st = in_sh + (k & (S - 1)) * SH::kInBytes;
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
       mbar_expect_tx(bar, 0);  // completes the stage's phase with no copy (the debug build's skip)
       return;
     }
-    if (((it ^ k) & 1) != 0) {
+    if (ord.is_v(it, k)) {
       mbar_expect_tx(bar, 128 * VB + 64);
       bulk_load(st, p.v_codes + irow * (D * VB / 8), 128 * VB, bar);
       bulk_load(st + SH::kScaleOff, p.v_scales + irow * (D / 32), 64, bar);
@@ -251,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
   int k = 0;
   bool ok = true;
   for (;; ++k) {
-    const int it = gw + k * n_warps;
+    const int it = ord.item(k);
     if (it >= items) break;
-    const bool is_v = ((it ^ k) & 1) != 0;
+    const bool is_v = ord.is_v(it, k);
     const uint32_t st = in_sh + (k & (S - 1)) * SH::kInBytes;
     if (!__all_sync(kFull, mbar_wait(bar_sh + 8 * (k & (S - 1)), (k / S) & 1, kBulkWaitLimit))) {
       ok = false;  // the same decision in every lane
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) {
-      const int r0 = (it >> 1) * G::RPW;
+      const int r0 = ord.tile(it) * G::RPW;
       bulk_store(static_cast<__nv_bfloat16*>(is_v ? p.v_out : p.k_out) + static_cast<size_t>(r0) * D, ob,
                  SH::kOutBytes);
       bulk_commit();
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, (BulkDecodeShape<D, VB, KMODE>::kMin
     if (lane == 0 && p.err != nullptr) atomicOr(p.err, 1u);
     // wait (bounded) for this warp's loads still in flight before leaving
     for (int j = k; j < k + S; ++j) {
-      if (gw + j * n_warps >= items) break;
+      if (ord.item(j) >= items) break;
       if (!mbar_wait(bar_sh + 8 * (j & (S - 1)), (j / S) & 1, kBulkWaitLimit)) break;
     }
   }
@@ -328,10 +335,15 @@ inline bool bulk_decode_ok(const DecodeParams& p, bool out_bf16) {
 template <int D, int VB, int KMODE, bool ROT>
 cudaError_t launch_decode_bulk(const DecodeParams& p, cudaStream_t s) {
   using SH = BulkDecodeShape<D, VB, KMODE>;
-  static const int resident = prepare_dyn_smem(decode_bulk_kernel<D, VB, KMODE, ROT>, SH::kSmem);
+  static const int resident =
+      std::min(prepare_dyn_smem(decode_bulk_kernel<D, VB, KMODE, ROT, false>, SH::kSmem),
+               prepare_dyn_smem(decode_bulk_kernel<D, VB, KMODE, ROT, true>, SH::kSmem));
   const long long items = 2LL * (p.rows / Geo<D>::RPW);
   const int grid = grid_for(items, resident);
-  const cudaError_t e = launch_pdl(decode_bulk_kernel<D, VB, KMODE, ROT>, grid, p, s, SH::kSmem);
+  // short launches (at most kSnakeSteps steps per warp) take the snake order
+  const bool snake = items <= static_cast<long long>(kSnakeSteps) * grid * SH::kWarps;
+  const cudaError_t e = snake ? launch_pdl(decode_bulk_kernel<D, VB, KMODE, ROT, true>, grid, p, s, SH::kSmem)
+                              : launch_pdl(decode_bulk_kernel<D, VB, KMODE, ROT, false>, grid, p, s, SH::kSmem);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
